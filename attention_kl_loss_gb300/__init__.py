@@ -1,0 +1,22 @@
+"""GB300-native (sm_103a) attention-KL primitive: KL(P1 || P2) between a
+teacher and a student attention distribution per query row, with gradients,
+without materialising the N_Q x N_K score or probability matrices.
+
+The computation lives in the CUDA library built from ``csrc/`` (C ABI in
+``include/streamkl.h``); this package only marshals arguments to it.
+"""
+from .binding import (  # noqa: F401
+    StreamKLError,
+    choose_splits,
+    load,
+    new_status,
+    raise_on_device_status,
+    selftest_wait_timeout,
+    streamkl_bwd,
+    streamkl_bwd_workspace_size,
+    streamkl_fwd,
+    streamkl_fwd_workspace_size,
+    streamkl_workspace_size,
+)
+
+__version__ = "0.1.0"

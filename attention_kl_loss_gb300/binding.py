@@ -1,0 +1,201 @@
+"""ctypes binding of the C ABI in ``include/streamkl.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library. PyTorch provides device memory and the current stream. The library
+must have been built in-tree (``__graft_entry__.build()`` or
+``python -m attention_kl_loss_gb300.build``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+STREAMKL_OK = 0
+STREAMKL_ERR_INVALID_ARG = 1
+STREAMKL_ERR_UNSUPPORTED = 2
+STREAMKL_ERR_CUDA = 3
+STREAMKL_ERR_TIMEOUT = 4
+
+_lib: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_Z = ctypes.c_size_t
+
+_SIGNATURES = {
+    "streamkl_status_string": (ctypes.c_char_p, [_I]),
+    "streamkl_last_error": (ctypes.c_char_p, []),
+    "streamkl_choose_splits": (_I, [_I, _I, _I, _I, _I, _I]),
+    "streamkl_fwd_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "streamkl_bwd_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "streamkl_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
+    "streamkl_fwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P, _P, _Z,
+                          _P, _P]),
+    "streamkl_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _P,
+                          _P, _P, _P, _Z, _P, _P]),
+    "streamkl_selftest_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
+}
+
+
+class StreamKLError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        name = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT"}.get(status, "?")
+        super().__init__(f"{where}: STREAMKL_ERR_{name} ({status}) {detail}".strip())
+
+
+def library_path() -> str:
+    return _build.lib_path()
+
+
+def load() -> ctypes.CDLL:
+    """Load the in-tree library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"StreamKL CUDA library not found at {path}; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream: Optional[torch.cuda.Stream]):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != STREAMKL_OK:
+        detail = load().streamkl_last_error().decode(errors="replace")
+        raise StreamKLError(status, where, detail)
+
+
+def _dims(q1, k1, q2, k2):
+    for name, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 4:
+            raise ValueError(f"{name} must be a 4-D tensor [B, H, N, d]")
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    B, H, NQ, d = q1.shape
+    NK = k1.shape[2]
+    if q2.shape != q1.shape or k1.shape != (B, H, NK, d) or k2.shape != k1.shape:
+        raise ValueError("shape mismatch: Q1,Q2 must be [B,H,NQ,d] and K1,K2 [B,H,NK,d]")
+    return B, H, NQ, NK, d
+
+
+def choose_splits(B, H, NQ, NK, d, causal) -> int:
+    return int(load().streamkl_choose_splits(B, H, NQ, NK, d, int(causal)))
+
+
+def streamkl_fwd_workspace_size(B, H, NQ, NK, d, causal, num_splits=0) -> int:
+    return int(load().streamkl_fwd_workspace_size(B, H, NQ, NK, d, int(causal), int(num_splits)))
+
+
+def streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal, want_grad1) -> int:
+    return int(load().streamkl_bwd_workspace_size(B, H, NQ, NK, d, int(causal), int(want_grad1)))
+
+
+def streamkl_workspace_size(B, H, NQ, NK, d, causal, want_grad1) -> int:
+    return int(load().streamkl_workspace_size(B, H, NQ, NK, d, int(causal), int(want_grad1)))
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word for the kernels' bounded waits."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def _workspace(nbytes: int, device, workspace):
+    if nbytes == 0:
+        return None
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace too small: need {nbytes} bytes")
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def streamkl_fwd(q1, k1, q2, k2, scale: Optional[float] = None, causal: bool = False,
+                 num_splits: int = 0, out=None, workspace=None, dev_status=None, stream=None):
+    """Per-row KL(P1||P2), lse1, lse2 (fp32 [B, H, N_Q]) via the CUDA library."""
+    lib = load()
+    B, H, NQ, NK, d = _dims(q1, k1, q2, k2)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dev = q1.device
+    if out is None:
+        out = tuple(torch.empty((B, H, NQ), dtype=torch.float32, device=dev) for _ in range(3))
+    kl, lse1, lse2 = out
+    need = streamkl_fwd_workspace_size(B, H, NQ, NK, d, causal, num_splits)
+    ws = _workspace(need, dev, workspace)
+    status = dev_status if dev_status is not None else new_status(dev)
+    st = lib.streamkl_fwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), B, H, NQ, NK, d, scale,
+                          int(causal), int(num_splits), _ptr(kl), _ptr(lse1), _ptr(lse2),
+                          _ptr(ws), need if ws is not None else 0, _ptr(status),
+                          _stream_handle(stream))
+    _check(st, "streamkl_fwd")
+    return kl, lse1, lse2
+
+
+def streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = None,
+                 causal: bool = False, grad1: bool = False, out=None, workspace=None,
+                 dev_status=None, stream=None):
+    """Gradients of sum(dkl * KL): (dq2, dk2, dq1, dk1), bf16; dq1/dk1 None
+    unless ``grad1``."""
+    lib = load()
+    B, H, NQ, NK, d = _dims(q1, k1, q2, k2)
+    for name, t in (("kl", kl), ("lse1", lse1), ("lse2", lse2), ("dkl", dkl)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.shape != (B, H, NQ):
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor [B, H, N_Q]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dev = q1.device
+    if out is None:
+        dq2 = torch.empty_like(q2)
+        dk2 = torch.empty_like(k2)
+        dq1 = torch.empty_like(q1) if grad1 else None
+        dk1 = torch.empty_like(k1) if grad1 else None
+    else:
+        dq2, dk2, dq1, dk1 = out
+    need = streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal, grad1)
+    ws = _workspace(need, dev, workspace)
+    status = dev_status if dev_status is not None else new_status(dev)
+    st = lib.streamkl_bwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), B, H, NQ, NK, d, scale,
+                          int(causal), _ptr(kl), _ptr(lse1), _ptr(lse2), _ptr(dkl), _ptr(dq2),
+                          _ptr(dk2), _ptr(dq1), _ptr(dk1), _ptr(ws), need, _ptr(status),
+                          _stream_handle(stream))
+    _check(st, "streamkl_bwd")
+    return dq2, dk2, dq1, dk1
+
+
+def selftest_wait_timeout(timeout_us: int = 20000, dev_status=None, stream=None) -> torch.Tensor:
+    """Run the bounded-wait self-test kernel; returns the status tensor."""
+    lib = load()
+    status = dev_status if dev_status is not None else new_status()
+    _check(lib.streamkl_selftest_wait_timeout(_ptr(status), int(timeout_us), _stream_handle(stream)),
+           "streamkl_selftest_wait_timeout")
+    return status
+
+
+def raise_on_device_status(dev_status: torch.Tensor, where: str = "kernel"):
+    """Synchronise and raise if a kernel recorded a failure in ``dev_status``."""
+    torch.cuda.synchronize(dev_status.device)
+    v = int(dev_status.item())
+    if v != 0:
+        raise StreamKLError(v, where, "a bounded wait inside the kernel gave up")

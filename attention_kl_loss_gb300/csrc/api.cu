@@ -1,0 +1,341 @@
+// C-ABI layer: argument checks, TMA tensor maps, split choice, launches.
+// No allocation, no synchronisation; everything is enqueued on the caller's
+// stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/streamkl.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+streamkl_status fail(streamkl_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+streamkl_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(STREAMKL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+uint64_t wait_timeout_ns() {
+  static uint64_t v = [] {
+    const char* s = std::getenv("STREAMKL_WAIT_TIMEOUT_MS");
+    long long ms = s ? std::atoll(s) : 2000;
+    if (ms < 1) ms = 1;
+    return static_cast<uint64_t>(ms) * 1000000ull;
+  }();
+  return v;
+}
+
+int num_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 152;
+  }
+  static int cache[64] = {0};
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    n = 152;
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+streamkl_status check_sizes(int B, int H, int NQ, int NK, int d, int causal) {
+  if (B < 1 || H < 1 || NQ < 1 || NK < 1)
+    return fail(STREAMKL_ERR_INVALID_ARG, "sizes must be >= 1 (B=%d H=%d NQ=%d NK=%d)", B, H, NQ, NK);
+  if (d != 64 && d != 128) return fail(STREAMKL_ERR_UNSUPPORTED, "head dim d=%d (supported: 64, 128)", d);
+  if (static_cast<long long>(B) * H > 65535)
+    return fail(STREAMKL_ERR_UNSUPPORTED, "B*H=%lld exceeds 65535", static_cast<long long>(B) * H);
+  if (NQ > (1 << 30) || NK > (1 << 30)) return fail(STREAMKL_ERR_UNSUPPORTED, "sequence length above 2^30");
+  if (causal != 0 && causal != 1) return fail(STREAMKL_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (causal && NQ > NK)
+    return fail(STREAMKL_ERR_INVALID_ARG, "causal needs NQ <= NK (bottom-right alignment), got NQ=%d NK=%d", NQ, NK);
+  return STREAMKL_OK;
+}
+
+int key_tiles(int NK) { return (NK + skl::kBlockN - 1) / skl::kBlockN; }
+
+// Choose the split count by a wave model: time ~ waves * tiles per split.
+int choose_splits_impl(int B, int H, int NQ, int NK) {
+  const long long ctas = static_cast<long long>((NQ + skl::kBlockM - 1) / skl::kBlockM) * B * H;
+  const int tiles = key_tiles(NK);
+  const int sms = num_sms();
+  if (ctas >= 8LL * sms) return 1;
+  const int smax = std::max(1, std::min(32, tiles / 4));
+  auto cost = [&](int s) {
+    const long long units = ctas * s;
+    const long long waves = (units + sms - 1) / sms;
+    const long long tps = (tiles + s - 1) / s;
+    return waves * tps;
+  };
+  int best = 1;
+  long long best_t = cost(1);
+  for (int s = 2; s <= smax; ++s) {
+    const long long t = cost(s);
+    if (t < best_t) {
+      best_t = t;
+      best = s;
+    }
+  }
+  if (best > 1 && static_cast<double>(best_t) > 0.95 * static_cast<double>(cost(1))) return 1;
+  return best;
+}
+
+// Effective split count and tiles per split for a requested count.
+void split_plan(int requested, int NK, int* splits, int* tps) {
+  const int tiles = key_tiles(NK);
+  int s = std::max(1, std::min(requested, tiles));
+  const int per = (tiles + s - 1) / s;
+  *tps = per;
+  *splits = (tiles + per - 1) / per;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t fwd_ws(int B, int H, int NQ, int splits) {
+  if (splits <= 1) return 0;
+  return align256(static_cast<size_t>(5) * splits * B * H * NQ * sizeof(float));
+}
+
+size_t bwd_ws(int B, int H, int NQ, int d, int grad1) {
+  const size_t one = align256(static_cast<size_t>(B) * H * NQ * d * sizeof(float));
+  return grad1 ? 2 * one : one;
+}
+
+streamkl_status make_map(CUtensorMap* m, const void* ptr, int BH, int N, int d, const char* name) {
+  auto enc = encode_fn();
+  if (!enc) return fail(STREAMKL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(d) * 2,
+                                 static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(skl::kBlockM), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim, gstride, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(STREAMKL_ERR_CUDA, "tensor map for %s failed (CUresult %d)", name, static_cast<int>(r));
+  return STREAMKL_OK;
+}
+
+streamkl_status check_inputs(const void* q1, const void* k1, const void* q2, const void* k2) {
+  const void* ps[4] = {q1, k1, q2, k2};
+  const char* names[4] = {"q1", "k1", "q2", "k2"};
+  for (int i = 0; i < 4; ++i) {
+    if (!ps[i]) return fail(STREAMKL_ERR_INVALID_ARG, "%s is NULL", names[i]);
+    if (!aligned16(ps[i])) return fail(STREAMKL_ERR_INVALID_ARG, "%s is not 16-byte aligned", names[i]);
+  }
+  return STREAMKL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* streamkl_status_string(streamkl_status s) {
+  switch (s) {
+    case STREAMKL_OK: return "STREAMKL_OK";
+    case STREAMKL_ERR_INVALID_ARG: return "STREAMKL_ERR_INVALID_ARG";
+    case STREAMKL_ERR_UNSUPPORTED: return "STREAMKL_ERR_UNSUPPORTED";
+    case STREAMKL_ERR_CUDA: return "STREAMKL_ERR_CUDA";
+    case STREAMKL_ERR_TIMEOUT: return "STREAMKL_ERR_TIMEOUT";
+  }
+  return "STREAMKL_ERR_UNKNOWN";
+}
+
+const char* streamkl_last_error(void) { return g_err; }
+
+int streamkl_choose_splits(int B, int H, int NQ, int NK, int d, int causal) {
+  if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return 0;
+  int s, tps;
+  split_plan(choose_splits_impl(B, H, NQ, NK), NK, &s, &tps);
+  return s;
+}
+
+size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal, int num_splits) {
+  if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK || num_splits < 0) return 0;
+  int s, tps;
+  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK), NK, &s, &tps);
+  return fwd_ws(B, H, NQ, s);
+}
+
+size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
+  if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return 0;
+  return bwd_ws(B, H, NQ, d, want_grad1 ? 1 : 0);
+}
+
+size_t streamkl_workspace_size(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
+  const size_t a = streamkl_fwd_workspace_size(B, H, NQ, NK, d, causal, 0);
+  const size_t b = streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal, want_grad1);
+  return a > b ? a : b;
+}
+
+streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2, int B,
+                             int H, int NQ, int NK, int d, float scale, int causal, int num_splits,
+                             float* kl, float* lse1, float* lse2, void* workspace, size_t ws_bytes,
+                             int* dev_status, void* stream) {
+  g_err[0] = '\0';
+  streamkl_status st = check_sizes(B, H, NQ, NK, d, causal);
+  if (st != STREAMKL_OK) return st;
+  if ((st = check_inputs(q1, k1, q2, k2)) != STREAMKL_OK) return st;
+  if (!kl || !lse1 || !lse2) return fail(STREAMKL_ERR_INVALID_ARG, "kl/lse1/lse2 must be non-NULL");
+  if (!dev_status) return fail(STREAMKL_ERR_INVALID_ARG, "dev_status must be non-NULL");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(STREAMKL_ERR_INVALID_ARG, "scale must be finite and > 0");
+  if (num_splits < 0) return fail(STREAMKL_ERR_INVALID_ARG, "num_splits must be >= 0");
+  int splits, tps;
+  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK), NK, &splits, &tps);
+  const size_t need = fwd_ws(B, H, NQ, splits);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
+    return fail(STREAMKL_ERR_INVALID_ARG, "forward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
+
+  const int BH = B * H;
+  CUtensorMap mq1, mk1, mq2, mk2;
+  if ((st = make_map(&mq1, q1, BH, NQ, d, "q1")) != STREAMKL_OK) return st;
+  if ((st = make_map(&mk1, k1, BH, NK, d, "k1")) != STREAMKL_OK) return st;
+  if ((st = make_map(&mq2, q2, BH, NQ, d, "q2")) != STREAMKL_OK) return st;
+  if ((st = make_map(&mk2, k2, BH, NK, d, "k2")) != STREAMKL_OK) return st;
+
+  skl::FwdArgs a{};
+  a.tm_q1 = &mq1;
+  a.tm_k1 = &mk1;
+  a.tm_q2 = &mq2;
+  a.tm_k2 = &mk2;
+  a.BH = BH;
+  a.NQ = NQ;
+  a.NK = NK;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.kl = kl;
+  a.lse1 = lse1;
+  a.lse2 = lse2;
+  a.part = splits > 1 ? static_cast<float*>(workspace) : nullptr;
+  a.splits = splits;
+  a.tiles_per_split = tps;
+  a.dev_status = dev_status;
+  a.timeout_ns = wait_timeout_ns();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = skl::launch_fwd(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  if (splits > 1) {
+    e = skl::launch_fwd_combine(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
+  }
+  return STREAMKL_OK;
+}
+
+streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2, int B,
+                             int H, int NQ, int NK, int d, float scale, int causal, const float* kl,
+                             const float* lse1, const float* lse2, const float* dkl, void* dq2,
+                             void* dk2, void* dq1, void* dk1, void* workspace, size_t ws_bytes,
+                             int* dev_status, void* stream) {
+  g_err[0] = '\0';
+  streamkl_status st = check_sizes(B, H, NQ, NK, d, causal);
+  if (st != STREAMKL_OK) return st;
+  if ((st = check_inputs(q1, k1, q2, k2)) != STREAMKL_OK) return st;
+  if (!kl || !lse1 || !lse2 || !dkl) return fail(STREAMKL_ERR_INVALID_ARG, "kl/lse1/lse2/dkl must be non-NULL");
+  if (!dq2 || !dk2) return fail(STREAMKL_ERR_INVALID_ARG, "dq2 and dk2 must be non-NULL");
+  if ((dq1 == nullptr) != (dk1 == nullptr))
+    return fail(STREAMKL_ERR_INVALID_ARG, "dq1 and dk1 must be both NULL or both non-NULL");
+  if (!aligned16(dq2) || !aligned16(dk2) || (dq1 && (!aligned16(dq1) || !aligned16(dk1))))
+    return fail(STREAMKL_ERR_INVALID_ARG, "gradient outputs must be 16-byte aligned");
+  if (!dev_status) return fail(STREAMKL_ERR_INVALID_ARG, "dev_status must be non-NULL");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(STREAMKL_ERR_INVALID_ARG, "scale must be finite and > 0");
+  const int grad1 = dq1 != nullptr;
+  const size_t need = bwd_ws(B, H, NQ, d, grad1);
+  if (!workspace || ws_bytes < need || !aligned16(workspace))
+    return fail(STREAMKL_ERR_INVALID_ARG, "backward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
+
+  const int BH = B * H;
+  CUtensorMap mq1, mk1, mq2, mk2;
+  if ((st = make_map(&mq1, q1, BH, NQ, d, "q1")) != STREAMKL_OK) return st;
+  if ((st = make_map(&mk1, k1, BH, NK, d, "k1")) != STREAMKL_OK) return st;
+  if ((st = make_map(&mq2, q2, BH, NQ, d, "q2")) != STREAMKL_OK) return st;
+  if ((st = make_map(&mk2, k2, BH, NK, d, "k2")) != STREAMKL_OK) return st;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, need, s);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
+  const size_t one = need / (grad1 ? 2 : 1);
+  skl::BwdArgs a{};
+  a.tm_q1 = &mq1;
+  a.tm_k1 = &mk1;
+  a.tm_q2 = &mq2;
+  a.tm_k2 = &mk2;
+  a.BH = BH;
+  a.NQ = NQ;
+  a.NK = NK;
+  a.d = d;
+  a.causal = causal;
+  a.grad1 = grad1;
+  a.scale = scale;
+  a.kl = kl;
+  a.lse1 = lse1;
+  a.lse2 = lse2;
+  a.g = dkl;
+  a.dq2acc = static_cast<float*>(workspace);
+  a.dq1acc = grad1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + one) : nullptr;
+  a.dk2 = dk2;
+  a.dk1 = dk1;
+  a.dev_status = dev_status;
+  a.timeout_ns = wait_timeout_ns();
+  e = skl::launch_bwd(a, s);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  const long long n = static_cast<long long>(BH) * NQ * d;
+  e = skl::launch_dq_convert(a.dq2acc, dq2, n, s);
+  if (e != cudaSuccess) return cuda_fail(e, "dq2 convert launch");
+  if (grad1) {
+    e = skl::launch_dq_convert(a.dq1acc, dq1, n, s);
+    if (e != cudaSuccess) return cuda_fail(e, "dq1 convert launch");
+  }
+  return STREAMKL_OK;
+}
+
+streamkl_status streamkl_selftest_wait_timeout(int* dev_status, unsigned timeout_us, void* stream) {
+  g_err[0] = '\0';
+  if (!dev_status) return fail(STREAMKL_ERR_INVALID_ARG, "dev_status must be non-NULL");
+  if (timeout_us < 1 || timeout_us > 5000000u)
+    return fail(STREAMKL_ERR_INVALID_ARG, "timeout_us must be in [1, 5e6]");
+  cudaError_t e = skl::launch_wait_selftest(dev_status, static_cast<uint64_t>(timeout_us) * 1000ull,
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return STREAMKL_OK;
+}
+
+}  // extern "C"

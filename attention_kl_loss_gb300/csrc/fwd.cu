@@ -1,0 +1,403 @@
+// Forward pass of the attention-KL primitive: one streaming pass over key
+// tiles that keeps, per query row, the coupled online state of the pages'
+// online formulation (gist.science technical summary, "Metodologia" section 1):
+// running maxima m1, m2, exponential sums l1, l2 and the rescaled running sum
+// acc = sum_j exp(s1_j - m1) (s1_j - s2_j). At the end
+//     LSE_t = m_t + log l_t,   KL = acc / l1 + LSE2 - LSE1.
+// S1 and S2 never leave the SM: they are produced by tcgen05 MMAs into TMEM
+// and read back by the softmax warps. Key tiles past a row block's causal
+// frontier are never loaded (same section: masked tiles are skipped).
+//
+// CTA layout (384 threads, one CTA per SM because of shared memory):
+//   warp 0       TMA producer: Q1/Q2 tile once, K1/K2 tiles through a ring
+//   warp 1       TMEM owner + MMA issuer: S1 = Q1 K1^T, S2 = Q2 K2^T per tile,
+//                double-buffered in TMEM (2 x 256 columns)
+//   warps 4..11  two softmax warpgroups; thread = one query row (TMEM lane);
+//                warpgroup w owns key columns [64w, 64w+64) of every tile and
+//                keeps its own five-scalar state; the two states are merged
+//                at the end exactly like split-K partials.
+//
+// Numerics: exponentials are base 2 with the reference maximum kept in log2
+// units (r = m * scale * log2 e). The reference is only moved when a chunk's
+// maximum exceeds it by more than kTau (=8, so no term exceeds 2^8); moving it
+// rescales l and acc, so the result is the same for any reference.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace skl {
+
+namespace {
+
+constexpr int kFwdThreads = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kTau = 8.0f;
+
+template <int D>
+struct FwdLayout {
+  static constexpr int KB = D / 64;          // 64-column (128-byte) boxes per row
+  static constexpr int TILE = kBlockM * D * 2;  // one 128-row bf16 tile
+  static constexpr int STAGES = D == 128 ? 2 : 4;
+  static constexpr int OFF_Q1 = 0;
+  static constexpr int OFF_Q2 = TILE;
+  static constexpr int OFF_K = 2 * TILE;  // stage s: K1 at +2s*TILE, K2 at +(2s+1)*TILE
+  static constexpr int OFF_BAR = OFF_K + STAGES * 2 * TILE;
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], s_empty[2], drain
+  static constexpr int NBAR = 1 + 2 * STAGES + 4 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
+  static constexpr int OFF_XCH = OFF_MISC + 16;        // [5][128] floats
+  static constexpr int BYTES = OFF_XCH + 5 * kBlockM * 4;
+  static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024
+};
+
+struct RowState {
+  float r1, l1, r2, l2, acc;  // r_t in log2 units; acc in raw dot-product units
+};
+
+// Fold one 64-column chunk of a row into the state. a = S1 row values, b = S2
+// (raw dot products). With MASK, keys >= lim are excluded.
+template <bool MASK>
+__device__ __forceinline__ void fold_chunk(float (&a)[64], float (&b)[64], int key0, int lim,
+                                           float c, RowState& st) {
+  if (MASK) {
+#pragma unroll
+    for (int k = 0; k < 64; ++k) {
+      if (key0 + k >= lim) {
+        a[k] = -INFINITY;
+        b[k] = -INFINITY;
+      }
+    }
+  }
+  float x1[22], x2[22];
+#pragma unroll
+  for (int k = 0; k < 21; ++k) {
+    x1[k] = max3(a[3 * k], a[3 * k + 1], a[3 * k + 2]);
+    x2[k] = max3(b[3 * k], b[3 * k + 1], b[3 * k + 2]);
+  }
+  x1[21] = a[63];
+  x2[21] = b[63];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) {
+    x1[k] = max3(x1[3 * k], x1[3 * k + 1], x1[3 * k + 2]);
+    x2[k] = max3(x2[3 * k], x2[3 * k + 1], x2[3 * k + 2]);
+  }
+  float cm1 = max3(max3(x1[0], x1[1], x1[2]), max3(x1[3], x1[4], x1[5]), fmaxf(x1[6], x1[21]));
+  float cm2 = max3(max3(x2[0], x2[1], x2[2]), max3(x2[3], x2[4], x2[5]), fmaxf(x2[6], x2[21]));
+  if (MASK && cm1 == -INFINITY) return;  // no allowed key in this chunk
+  const float t1 = cm1 * c, t2 = cm2 * c;
+  if (t1 > st.r1 + kTau) {
+    const float al = ex2(st.r1 - t1);
+    st.l1 *= al;
+    st.acc *= al;
+    st.r1 = t1;
+  }
+  if (t2 > st.r2 + kTau) {
+    st.l2 *= ex2(st.r2 - t2);
+    st.r2 = t2;
+  }
+  float l1p[4] = {0.f, 0.f, 0.f, 0.f}, l2p[4] = {0.f, 0.f, 0.f, 0.f}, ap[4] = {0.f, 0.f, 0.f, 0.f};
+  const float nr1 = -st.r1, nr2 = -st.r2;
+#pragma unroll
+  for (int k = 0; k < 64; ++k) {
+    const float p1 = ex2(fmaf(a[k], c, nr1));
+    const float p2 = ex2(fmaf(b[k], c, nr2));
+    l1p[k & 3] += p1;
+    l2p[k & 3] += p2;
+    float dd = a[k] - b[k];
+    if (MASK) dd = (a[k] == -INFINITY) ? 0.f : dd;
+    ap[k & 3] = fmaf(p1, dd, ap[k & 3]);
+  }
+  st.l1 += (l1p[0] + l1p[1]) + (l1p[2] + l1p[3]);
+  st.l2 += (l2p[0] + l2p[1]) + (l2p[2] + l2p[3]);
+  st.acc += (ap[0] + ap[1]) + (ap[2] + ap[3]);
+}
+
+// Merge state y into x (same row, disjoint key sets).
+__device__ __forceinline__ void merge_state(RowState& x, const RowState& y) {
+  const float R1 = fmaxf(x.r1, y.r1), R2 = fmaxf(x.r2, y.r2);
+  if (R1 == -INFINITY) return;  // neither side saw an allowed key
+  const float wx1 = ex2(x.r1 - R1), wy1 = ex2(y.r1 - R1);
+  const float wx2 = ex2(x.r2 - R2), wy2 = ex2(y.r2 - R2);
+  x.l1 = x.l1 * wx1 + y.l1 * wy1;
+  x.acc = x.acc * wx1 + y.acc * wy1;
+  x.l2 = x.l2 * wx2 + y.l2 * wy2;
+  x.r1 = R1;
+  x.r2 = R2;
+}
+
+__device__ __forceinline__ void finish_row(const RowState& s, float scale, float& kl, float& lse1,
+                                           float& lse2) {
+  lse1 = (s.r1 + log2f(s.l1)) * kLn2;
+  lse2 = (s.r2 + log2f(s.l2)) * kLn2;
+  kl = scale * (s.acc / s.l1) - lse1 + lse2;
+}
+
+template <int D, bool SPLIT>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    streamkl_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1,
+                        const __grid_constant__ CUtensorMap tm_k1,
+                        const __grid_constant__ CUtensorMap tm_q2,
+                        const __grid_constant__ CUtensorMap tm_k2, int NQ, int NK, int causal,
+                        float scale, float* __restrict__ kl_out, float* __restrict__ lse1_out,
+                        float* __restrict__ lse2_out, float* __restrict__ part, int splits,
+                        int tiles_per_split, int BH, int* dev_status, uint64_t timeout_ns) {
+  using L = FwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* gb = smem_raw + (sb - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const int nqb = (NQ + kBlockM - 1) / kBlockM;
+  const int qb = causal ? (nqb - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int split = static_cast<int>(blockIdx.y);
+  const int bh = static_cast<int>(blockIdx.z);
+  const int off = NK - NQ;
+  const int row_hi = min(NQ, (qb + 1) * kBlockM);  // exclusive
+  const int klim_blk = causal ? min(NK, row_hi + off) : NK;
+  const int n_tiles = (klim_blk + kBlockN - 1) / kBlockN;
+  const int t_begin = SPLIT ? split * tiles_per_split : 0;
+  const int t_end = SPLIT ? min(n_tiles, t_begin + tiles_per_split) : n_tiles;
+  int n_iter = max(0, t_end - t_begin);
+
+  const uint32_t bar0 = sb + L::OFF_BAR;
+  const uint32_t q_full = bar0;
+  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + L::STAGES + s); };
+  auto s_full = [&](int k) { return bar0 + 8u * (1 + 2 * L::STAGES + k); };
+  auto s_empty = [&](int k) { return bar0 + 8u * (3 + 2 * L::STAGES + k); };
+  const uint32_t drain = bar0 + 8u * (5 + 2 * L::STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
+  volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < L::STAGES; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
+    }
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(s_full(k), 1);
+      mbar_init(s_empty(k), 8);  // one arrival per softmax warp
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    // a failure recorded earlier (this launch or a previous one) skips the work
+    *skip_flag = *reinterpret_cast<volatile int*>(dev_status) != 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q1);
+    tma_prefetch_desc(&tm_k1);
+    tma_prefetch_desc(&tm_q2);
+    tma_prefetch_desc(&tm_k2);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (*skip_flag) n_iter = 0;
+  const WaitCtx wc{abort_flag, dev_status, timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_iter > 0) {
+      mbar_arrive_expect_tx(q_full, 2 * L::TILE);
+#pragma unroll
+      for (int kb = 0; kb < L::KB; ++kb) {
+        tma_load_3d(sb + L::OFF_Q1 + kb * 16384, &tm_q1, q_full, kb * 64, qb * kBlockM, bh);
+        tma_load_3d(sb + L::OFF_Q2 + kb * 16384, &tm_q2, q_full, kb * 64, qb * kBlockM, bh);
+      }
+      int it = 0;
+      for (; it < n_iter; ++it) {
+        const int s = it % L::STAGES;
+        const uint32_t ph = (it / L::STAGES) & 1;
+        if (!wait_bounded(kv_empty(s), ph ^ 1, wc)) break;
+        mbar_arrive_expect_tx(kv_full(s), 2 * L::TILE);
+        const int krow = (t_begin + it) * kBlockN;
+        const uint32_t dst = sb + L::OFF_K + s * 2 * L::TILE;
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb) {
+          tma_load_3d(dst + kb * 16384, &tm_k1, kv_full(s), kb * 64, krow, bh);
+          tma_load_3d(dst + L::TILE + kb * 16384, &tm_k2, kv_full(s), kb * 64, krow, bh);
+        }
+      }
+      // Let every copy this thread issued land before the CTA can exit.
+      wait_drain(q_full, 0, timeout_ns);
+      for (int j = max(0, it - L::STAGES); j < it; ++j)
+        wait_drain(kv_full(j % L::STAGES), (j / L::STAGES) & 1, timeout_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_iter > 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBlockM, kBlockN, 0, 0);
+      bool ok = wait_bounded(q_full, 0, wc);
+      tc_fence_after();
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int s = it % L::STAGES;
+        const uint32_t ph = (it / L::STAGES) & 1;
+        const int slot = it & 1;
+        const uint32_t sph = (it >> 1) & 1;
+        if (!wait_bounded(kv_full(s), ph, wc)) break;
+        if (!wait_bounded(s_empty(slot), sph ^ 1, wc)) break;
+        tc_fence_after();
+        const uint32_t kbase = sb + L::OFF_K + s * 2 * L::TILE;
+        const uint32_t d1 = tmem + slot * 256, d2 = d1 + 128;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_bf16(d1, smem_desc_sw128(sb + L::OFF_Q1 + koff, 16, 1024),
+                   smem_desc_sw128(kbase + koff, 16, 1024), idesc, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_bf16(d2, smem_desc_sw128(sb + L::OFF_Q2 + koff, 16, 1024),
+                   smem_desc_sw128(kbase + L::TILE + koff, 16, 1024), idesc, k > 0);
+        }
+        mma_commit(s_full(slot));
+        mma_commit(kv_empty(s));
+      }
+      mma_commit(drain);
+      wait_drain(drain, 0, timeout_ns);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax / KL
+    const int wg = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qrow = qb * kBlockM + r;
+    const float c = scale * kLog2e;
+    const int lim = causal ? min(NK, qrow + 1 + off) : NK;
+    RowState st{-INFINITY, 0.f, -INFINITY, 0.f, 0.f};
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * 64;
+    for (int it = 0; it < n_iter; ++it) {
+      const int slot = it & 1;
+      const uint32_t sph = (it >> 1) & 1;
+      if (!wait_bounded(s_full(slot), sph, wc)) break;
+      tc_fence_after();
+      float a[64], b[64];
+      const uint32_t ta = lane_base + slot * 256;
+      tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(&a[0]));
+      tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
+      tmem_ld32(ta + 128, *reinterpret_cast<float(*)[32]>(&b[0]));
+      tmem_ld32(ta + 160, *reinterpret_cast<float(*)[32]>(&b[32]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty(slot));
+      const int key0 = (t_begin + it) * kBlockN + wg * 64;
+      if (key0 + 64 <= lim)
+        fold_chunk<false>(a, b, key0, lim, c, st);
+      else
+        fold_chunk<true>(a, b, key0, lim, c, st);
+    }
+    // merge the two column halves of each row
+    float* xch = reinterpret_cast<float*>(gb + L::OFF_XCH);
+    if (wg == 1) {
+      xch[0 * kBlockM + r] = st.r1;
+      xch[1 * kBlockM + r] = st.l1;
+      xch[2 * kBlockM + r] = st.r2;
+      xch[3 * kBlockM + r] = st.l2;
+      xch[4 * kBlockM + r] = st.acc;
+    }
+    named_bar_sync(1, 256);
+    if (wg == 0) {
+      const RowState other{xch[0 * kBlockM + r], xch[1 * kBlockM + r], xch[2 * kBlockM + r],
+                           xch[3 * kBlockM + r], xch[4 * kBlockM + r]};
+      merge_state(st, other);
+      if (qrow < NQ) {
+        const size_t o = static_cast<size_t>(bh) * NQ + qrow;
+        if (SPLIT) {
+          const size_t plane = static_cast<size_t>(BH) * NQ;
+          const size_t base = static_cast<size_t>(split) * plane + o;
+          const size_t fstride = static_cast<size_t>(splits) * plane;
+          part[0 * fstride + base] = st.r1;
+          part[1 * fstride + base] = st.l1;
+          part[2 * fstride + base] = st.r2;
+          part[3 * fstride + base] = st.l2;
+          part[4 * fstride + base] = st.acc;
+        } else {
+          float kl, l1, l2;
+          finish_row(st, scale, kl, l1, l2);
+          kl_out[o] = kl;
+          lse1_out[o] = l1;
+          lse2_out[o] = l2;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// One thread per (bh, row): merge the split partial states and finish.
+__global__ void streamkl_fwd_combine_kernel(const float* __restrict__ part, int splits,
+                                            long long plane, float scale,
+                                            float* __restrict__ kl_out,
+                                            float* __restrict__ lse1_out,
+                                            float* __restrict__ lse2_out) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= plane) return;
+  const long long fstride = static_cast<long long>(splits) * plane;
+  RowState st{-INFINITY, 0.f, -INFINITY, 0.f, 0.f};
+  for (int s = 0; s < splits; ++s) {
+    const long long b = s * plane + i;
+    const RowState y{part[b], part[fstride + b], part[2 * fstride + b], part[3 * fstride + b],
+                     part[4 * fstride + b]};
+    merge_state(st, y);
+  }
+  float kl, l1, l2;
+  finish_row(st, scale, kl, l1, l2);
+  kl_out[i] = kl;
+  lse1_out[i] = l1;
+  lse2_out[i] = l2;
+}
+
+template <int D, bool SPLIT>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+  using L = FwdLayout<D>;
+  auto kern = streamkl_fwd_kernel<D, SPLIT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  if (e != cudaSuccess) return e;
+  const int nqb = (a.NQ + kBlockM - 1) / kBlockM;
+  dim3 grid(nqb, SPLIT ? a.splits : 1, a.BH);
+  kern<<<grid, kFwdThreads, L::ALLOC, stream>>>(*a.tm_q1, *a.tm_k1, *a.tm_q2, *a.tm_k2, a.NQ, a.NK,
+                                                a.causal, a.scale, a.kl, a.lse1, a.lse2, a.part,
+                                                a.splits, a.tiles_per_split, a.BH, a.dev_status,
+                                                a.timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fwd_smem_bytes(int d) {
+  return d == 128 ? FwdLayout<128>::ALLOC : FwdLayout<64>::ALLOC;
+}
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  const bool split = a.splits > 1;
+  if (a.d == 128) return split ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
+  return split ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+}
+
+cudaError_t launch_fwd_combine(const FwdArgs& a, cudaStream_t stream) {
+  const long long plane = static_cast<long long>(a.BH) * a.NQ;
+  const int threads = 256;
+  const long long blocks = (plane + threads - 1) / threads;
+  streamkl_fwd_combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      a.part, a.splits, plane, a.scale, a.kl, a.lse1, a.lse2);
+  return cudaGetLastError();
+}
+
+}  // namespace skl

@@ -1,0 +1,443 @@
+#!/usr/bin/env python
+"""Benchmark of the attention-KL primitive (forward + backward) on GB300.
+
+One step = streamkl_fwd + streamkl_bwd (both gradient sets) over one batch of
+the 64K-context causal workload: B=1, H=32, N_Q=N_K=65536, d=128, bf16,
+teacher ~ N(0,1), student = teacher + 0.2 N(0,1), scale = 1/sqrt(128).
+
+Metric: fwd+bwd TFLOP/s at that workload with the usual attention convention,
+4 N_Q N_K d (forward) + 8 N_Q N_K d (backward) per head, halved for causal.
+The value is device-timed with inputs resident in HBM (inputs are 2 GiB, far
+larger than the 129 MB L2, so no flush is needed between steps). ``e2e`` is
+the same metric through the public Python API with host (pinned) buffers:
+each step copies the inputs in and the per-row KL out.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload per step).
+
+Under torchrun (N > 1) every rank runs its own replica of the workload on its
+own GPU (heads and batches are independent, so there is no exchange step);
+the reported time is the maximum over ranks and the value counts all ranks'
+work ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "causal64k"
+METRIC = "attention-KL fwd+bwd TFLOP/s and ms at 64K causal; % of GB300 BF16 tensor peak"
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    p.add_argument("--workload", default=WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget-s", type=float, default=15.0,
+                   help="target CPU seconds for the oracle sample")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args(argv)
+
+
+# --------------------------------------------------------------------------- ranks
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a host float over all ranks (identity on one rank)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_seed(rank: int) -> int:
+    """Each rank draws its own replica of the workload."""
+    return 1000 + rank
+
+
+# --------------------------------------------------------------------------- work counts
+def flop_counts(w):
+    """(fwd, bwd_metric, bwd_work, fwd_exact, bwd_work_exact) FLOPs for one step."""
+    bh = w.B * w.H
+    dense = w.NQ * w.NK * w.d * bh
+    half = 0.5 if w.causal else 1.0
+    pairs = w.live_pairs_per_head() * bh
+    fwd = 4 * dense * half
+    bwd_metric = 8 * dense * half
+    g = 12 if w.grad1 else 8
+    return fwd, bwd_metric, g * dense * half, 4 * pairs * w.d, g * pairs * w.d
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.flush()
+        self.out.seek(0)
+        rows = [r.strip().split(",") for r in self.out.read().splitlines() if r.strip()]
+        os.unlink(self.out.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                r = [x.strip() for x in r]
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+                for n, v in zip(names, r[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s, p in zip(sm, power) if p >= 0.5 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+def oracle_sample(w, budget_s: float, seed: int = 7):
+    """Time the fp64 oracle (fwd + bwd, both gradient sets) on the last R query
+    rows of one head, growing R until the sample takes ~budget_s seconds.
+    Returns (tflops, seconds, flops, description)."""
+    import numpy as np
+    from oracle import streamkl_oracle as orc
+
+    rng = np.random.default_rng(seed)
+
+    def bf16(x):
+        # round fp32 draws to bf16 (nearest-even on the bit pattern)
+        u = x.astype(np.float32).view(np.uint32)
+        u = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+        return u.view(np.float32).astype(np.float64)
+
+    q1 = bf16(rng.standard_normal((w.NQ, w.d)) * w.teacher_std)
+    k1 = bf16(rng.standard_normal((w.NK, w.d)) * w.teacher_std)
+    q2 = bf16(q1 + w.noise * rng.standard_normal((w.NQ, w.d)))
+    k2 = bf16(k1 + w.noise * rng.standard_normal((w.NK, w.d)))
+    g = np.full(w.NQ, 1.0 / (w.B * w.H * w.NQ))
+    off = w.NK - w.NQ
+    r = 64
+    while True:
+        rows = np.arange(w.NQ - r, w.NQ)
+        t0 = time.perf_counter()
+        orc.head_forward(q1, k1, q2, k2, w.scale, w.causal, rows=rows)
+        orc.head_backward(q1, k1, q2, k2, w.scale, w.causal, g, w.grad1, rows=rows)
+        dt = time.perf_counter() - t0
+        pairs = int(np.sum(np.minimum(w.NK, rows + 1 + off))) if w.causal else r * w.NK
+        # metric convention on the exact pairs of the sample: (4 + 8) d per pair
+        flops = 12.0 * pairs * w.d
+        if dt >= budget_s / 3 or r >= w.NQ:
+            desc = (f"head 0 of a fresh draw, last {r} query rows (all their {pairs} visible "
+                    f"(query,key) pairs), forward + backward"
+                    f"{' with both gradient sets' if w.grad1 else ''}, fp64 numpy")
+            return flops / dt / 1e12, dt, flops, desc
+        r = min(w.NQ, r * 2)
+
+
+def cpu_cores():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:  # noqa: BLE001
+        pass
+    return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------- arms
+def emit(obj):
+    print(json.dumps(obj), flush=True)
+
+
+def reference_arm(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    budget = args.cpu_budget_s
+    for _ in range(args.warmup):
+        oracle_sample(w, min(budget, 2.0))
+    vals, times = [], []
+    desc = ""
+    for _ in range(args.steps):
+        v, dt, flops, desc = oracle_sample(w, budget / max(1, args.steps))
+        vals.append(v)
+        times.append(dt)
+    value = statistics.median(vals)
+    emit({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w)},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    })
+    return 0
+
+
+def describe(w):
+    return (f"{w.name}: B={w.B} H={w.H} N_Q={w.NQ} N_K={w.NK} d={w.d} "
+            f"{'causal' if w.causal else 'non-causal'}, bf16 inputs, fwd+bwd"
+            f"{' incl. dQ1,dK1' if w.grad1 else ''}")
+
+
+def gpu_arm(args, w):
+    import torch
+    from attention_kl_loss_gb300 import binding, synthetic
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist_init("nccl")
+    binding.load()
+    q1, k1, q2, k2, g = synthetic.make_inputs(w, replica_seed(rank), dev)
+    B, H, NQ, NK, d = w.B, w.H, w.NQ, w.NK, w.d
+    ws_bytes = binding.streamkl_workspace_size(B, H, NQ, NK, d, w.causal, w.grad1)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    status = binding.new_status(dev)
+    kl, l1, l2 = (torch.empty((B, H, NQ), dtype=torch.float32, device=dev) for _ in range(3))
+    grads = (torch.empty_like(q2), torch.empty_like(k2),
+             torch.empty_like(q1) if w.grad1 else None, torch.empty_like(k1) if w.grad1 else None)
+    splits = binding.choose_splits(B, H, NQ, NK, d, w.causal)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, out=(kl, l1, l2), workspace=ws,
+                             dev_status=status)
+        if ev is not None:
+            ev[1].record(stream)
+        binding.streamkl_bwd(q1, k1, q2, k2, kl, l1, l2, g, w.scale, w.causal, grad1=w.grad1,
+                             out=grads, workspace=ws, dev_status=status)
+        if ev is not None:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    binding.raise_on_device_status(status, "warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+    binding.raise_on_device_status(status, "timed region")
+    clocks = clk.summary()
+    ms_total = start.elapsed_time(stop)
+    ms_total = max_over_ranks(ms_total, dev)
+    ms_step = ms_total / args.steps
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+
+    f_fwd, f_bwd_metric, f_bwd_work, f_fwd_exact, f_bwd_exact = flop_counts(w)
+    step_flops = f_fwd + f_bwd_metric
+    value = world * step_flops / (ms_step * 1e-3) / 1e12
+    pk = peaks()
+    sustained = pk["bf16_tflops_sustained"]
+    # per-kernel rooflines; the backward launch (kernel + dQ convert) is the larger
+    fwd_tf = f_fwd_exact / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = f_bwd_exact / (bwd_ms * 1e-3) / 1e12
+    kernels = {
+        "streamkl_fwd_kernel": {"ms": fwd_ms, "algorithmic_tflop": f_fwd_exact / 1e12,
+                                "achieved_tflops": fwd_tf, "frac_of_measured_sustained": fwd_tf / sustained},
+        "streamkl_bwd_kernel": {"ms": bwd_ms, "algorithmic_tflop": f_bwd_exact / 1e12,
+                                "achieved_tflops": bwd_tf, "frac_of_measured_sustained": bwd_tf / sustained,
+                                "note": "includes the fp32->bf16 dQ conversion and workspace clear"},
+    }
+    dom = "streamkl_bwd_kernel" if bwd_ms >= fwd_ms else "streamkl_fwd_kernel"
+    dom_tf = kernels[dom]["achieved_tflops"]
+    roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": sustained,
+                "unit": "TFLOP/s", "frac": dom_tf / sustained, "traffic": None,
+                "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a long step)"}
+    launches_per_step = 1 + (1 if splits > 1 else 0) + 1 + (2 if w.grad1 else 1)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        v, dt, flops, desc = oracle_sample(w, args.cpu_budget_s)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": f"{desc}; {dt:.1f} s"}
+
+    extra_hbm = {
+        "workspace_bytes": ws_bytes,
+        "saved_state_bytes": 3 * B * H * NQ * 4,
+        "materialised_p1_p2_bytes_avoided": 2 * B * H * NQ * NK * 2,
+    }
+    if rank == 0:
+        emit({
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": describe(w), "B": B, "H": H, "N_Q": NQ, "N_K": NK, "d": d,
+                       "causal": w.causal, "grad1": w.grad1, "splits": splits,
+                       "flop_convention": "4 NQ NK d fwd + 8 NQ NK d bwd per head, halved for causal",
+                       "l2": "inputs (2 GiB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
+            "bwd_tflops_metric": f_bwd_metric / (bwd_ms * 1e-3) / 1e12,
+            "pct_of_measured_peak": {"value": value / world / pk["bf16_tflops"],
+                                     "fwd": f_fwd / (fwd_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                                     "bwd_metric": f_bwd_metric / (bwd_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                                     "peak": f"{pk['source']} bf16_tflops (burst)"},
+            "roofline": roofline, "kernels": kernels,
+            "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": launches_per_step * args.steps,
+            "extra_hbm": extra_hbm,
+        })
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
+    """Same metric through the public API with host buffers: every step copies
+    the inputs from pinned host memory and reads the per-row KL back."""
+    import torch
+    q1, k1, q2, k2, g = synthetic.make_inputs(w, replica_seed(rank) + 7, dev)
+    host_in = [t.cpu().pin_memory() for t in (q1, k1, q2, k2, g)]
+    del q1, k1, q2, k2, g
+    dev_in = [torch.empty_like(t, device=dev) for t in host_in]
+    kl_host = torch.empty((w.B, w.H, w.NQ), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        for hsrc, d in zip(host_in, dev_in):
+            d.copy_(hsrc, non_blocking=True)
+        kl, l1, l2 = binding.streamkl_fwd(*dev_in[:4], w.scale, w.causal)
+        binding.streamkl_bwd(*dev_in[:4], kl, l1, l2, dev_in[4], w.scale, w.causal, grad1=w.grad1)
+        kl_host.copy_(kl, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, dev)
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = kl_host.numel() * 4
+    return {"value": world * step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "attention_kl_loss_gb300.streamkl_fwd/streamkl_bwd (ctypes over the C ABI)"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    from attention_kl_loss_gb300 import synthetic
+    w = synthetic.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return reference_arm(args, w)
+    if args.warmup < 3:
+        print("note: fewer than 3 warm-up steps requested", file=sys.stderr)
+    return gpu_arm(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,134 @@
+/*
+ * streamkl.h -- C ABI of the GB300 (sm_103a) attention-KL primitive.
+ *
+ * The operation ("StreamKL: Fast and Memory-Efficient KL Divergence for
+ * Boosting Attention Distillation", abstract and gist.science technical
+ * summary): for every batch b, head h and query row i,
+ *
+ *     S_t = scale * Q_t K_t^T (+ causal mask),  P_t = softmax(S_t),  t = 1, 2
+ *     KL[b,h,i] = sum_j P1[i,j] * log(P1[i,j] / P2[i,j])
+ *
+ * with P1 the teacher and P2 the student, computed without ever writing the
+ * N_Q x N_K matrices S1, S2, P1, P2 to device memory.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Q1, Q2 are [B, H, N_Q, d] and K1, K2 are [B, H, N_K, d], bf16, dense,
+ *   row-major (d contiguous), 16-byte aligned device pointers. d is 64 or 128.
+ * - Per-row vectors (kl, lse1, lse2, dkl) are [B, H, N_Q] fp32, dense.
+ * - Causal masking is bottom-right aligned: key j is visible to query i iff
+ *   j <= i + (N_K - N_Q) (j <= i when N_Q == N_K); it needs N_Q <= N_K.
+ * - All pointers are device pointers owned by the caller. The library
+ *   allocates no memory, never synchronises, and enqueues all work on
+ *   `stream` (a cudaStream_t; NULL means the legacy default stream).
+ * - Synchronous argument errors return STREAMKL_ERR_INVALID_ARG or
+ *   STREAMKL_ERR_UNSUPPORTED before anything is enqueued; a failed launch
+ *   returns STREAMKL_ERR_CUDA. streamkl_last_error() gives the detail.
+ * - dev_status is a caller-owned device int the kernels write when a bounded
+ *   wait inside them gives up (STREAMKL_ERR_TIMEOUT); they never clear it.
+ *   Clear it before use and read it after synchronising the stream. Results
+ *   of a call that set it are undefined.
+ */
+#ifndef STREAMKL_H_
+#define STREAMKL_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  STREAMKL_OK = 0,
+  STREAMKL_ERR_INVALID_ARG = 1,
+  STREAMKL_ERR_UNSUPPORTED = 2,
+  STREAMKL_ERR_CUDA = 3,
+  STREAMKL_ERR_TIMEOUT = 4
+} streamkl_status;
+
+/* Human-readable name of a status code (static string). */
+const char* streamkl_status_string(streamkl_status s);
+
+/* Detail message of the last failing call on this host thread ("" if none). */
+const char* streamkl_last_error(void);
+
+/*
+ * Split count the forward pass uses when num_splits == 0 (split-K over the
+ * key dimension; gist.science technical summary, section 3 "Variante
+ * Split-K": keys are partitioned across thread blocks so that few query rows
+ * still fill the GPU). Returns >= 1; 0 on invalid sizes.
+ */
+int streamkl_choose_splits(int B, int H, int NQ, int NK, int d, int causal);
+
+/*
+ * Workspace bytes the forward pass needs with `num_splits` splits (0 = the
+ * automatic choice). The split partial states are five fp32 per (split, b, h,
+ * row): running maxima, exponential sums and the weighted-logit-difference
+ * accumulator. 0 when no split is used.
+ */
+size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal,
+                                   int num_splits);
+
+/*
+ * Workspace bytes the backward pass needs: one fp32 [B, H, N_Q, d] dQ
+ * accumulator per requested gradient set (two when want_grad1 != 0).
+ */
+size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal,
+                                   int want_grad1);
+
+/* max(forward with automatic splits, backward): one buffer serves both. */
+size_t streamkl_workspace_size(int B, int H, int NQ, int NK, int d, int causal,
+                               int want_grad1);
+
+/*
+ * Forward pass (gist.science technical summary, "Metodologia" section 1:
+ * online formulation; section 2 "Estado Guardado": only KL and the two
+ * log-sum-exps are saved).
+ *   in : q1, k1, q2, k2 (bf16, layout above); scale > 0; causal 0/1;
+ *        num_splits: 0 = automatic, >= 1 forces that many key splits
+ *        (clamped to the number of key tiles).
+ *   out: kl[b,h,i] = KL(P1 || P2) of row i (nats), lse1/lse2[b,h,i] =
+ *        log sum_j exp(S_t[i,j]) over the visible keys (fp32).
+ *   workspace: device buffer of ws_bytes >= streamkl_fwd_workspace_size(...)
+ *        (may be NULL when that is 0); contents need no initialisation.
+ */
+streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
+                             int B, int H, int NQ, int NK, int d, float scale, int causal,
+                             int num_splits, float* kl, float* lse1, float* lse2,
+                             void* workspace, size_t ws_bytes, int* dev_status, void* stream);
+
+/*
+ * Backward pass of L = sum_{b,h,i} dkl[b,h,i] * KL[b,h,i] (gist.science
+ * technical summary, section 2: probabilities regenerated tile by tile as
+ * P_t = exp(S_t - LSE_t); "Configuracion 1": P1 fixed, gradients to Q2, K2;
+ * "Configuracion 2": P2 fixed, gradients to Q1, K1; section 3 "Estabilidad
+ * Numerica": log(P1/P2) from logits and saved LSEs).
+ *   in : q1, k1, q2, k2, sizes, scale, causal exactly as given to streamkl_fwd;
+ *        kl, lse1, lse2 as produced by streamkl_fwd; dkl = upstream gradient
+ *        per row (fp32 [B, H, N_Q]).
+ *   out: dq2 [B,H,N_Q,d], dk2 [B,H,N_K,d] (bf16); dq1, dk1 likewise, or both
+ *        NULL to skip configuration 2 (one NULL and one not is an error).
+ *   workspace: ws_bytes >= streamkl_bwd_workspace_size(..., want_grad1); the
+ *        call clears the part it uses (stream-ordered).
+ */
+streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
+                             int B, int H, int NQ, int NK, int d, float scale, int causal,
+                             const float* kl, const float* lse1, const float* lse2,
+                             const float* dkl, void* dq2, void* dk2, void* dq1, void* dk1,
+                             void* workspace, size_t ws_bytes, int* dev_status, void* stream);
+
+/*
+ * Self-test of the bounded-wait path: launches one tiny kernel that waits on
+ * a barrier nothing arrives on, for timeout_us microseconds, then records
+ * STREAMKL_ERR_TIMEOUT in *dev_status and returns. No other state is touched.
+ * The paper has no counterpart; it exists so that the failure path of the
+ * kernels' waits can be tested without hanging a GPU.
+ */
+streamkl_status streamkl_selftest_wait_timeout(int* dev_status, unsigned timeout_us,
+                                               void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* STREAMKL_H_ */

@@ -1,0 +1,119 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every entry
+point the header declares, and its host logic (split choice, workspace sizes,
+argument validation) behaves as documented. No call here reaches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "streamkl.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_kl_loss_gb300 import build, binding
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(streamkl_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ["streamkl_fwd", "streamkl_bwd", "streamkl_workspace_size",
+                     "streamkl_status_string"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA",
+                                 "ERR_TIMEOUT"]):
+        assert lib.streamkl_status_string(code).decode() == "STREAMKL_" + name
+
+
+def test_split_choice(lib):
+    # 128 (b,h) x 4 query tiles over 1024 key tiles: 8 splits fill 152 SMs
+    assert lib.streamkl_choose_splits(4, 32, 512, 131072, 128, 1) == 8
+    # plenty of query tiles: no split
+    assert lib.streamkl_choose_splits(1, 32, 65536, 65536, 128, 1) == 1
+    assert lib.streamkl_choose_splits(2, 16, 4096, 4096, 128, 0) == 1
+    assert lib.streamkl_choose_splits(1, 8, 16384, 16384, 64, 0) == 1
+    # decode-like single row: split the keys
+    assert lib.streamkl_choose_splits(1, 32, 1, 65536, 128, 1) > 4
+    # invalid sizes
+    assert lib.streamkl_choose_splits(1, 1, 8, 4, 64, 1) == 0
+
+
+def test_workspace_sizes(lib):
+    assert lib.streamkl_fwd_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 5 * 8 * 128 * 512 * 4
+    assert lib.streamkl_fwd_workspace_size(4, 32, 512, 131072, 128, 1, 1) == 0
+    assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 1) == 2 * 32 * 65536 * 128 * 4
+    assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 0) == 32 * 65536 * 128 * 4
+    assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == max(
+        5 * 8 * 128 * 512 * 4, 128 * 512 * 128 * 4)
+
+
+def test_forced_split_workspace_rounding(lib):
+    # 100 rows, 2 key tiles, request 16 splits -> 2 effective splits
+    n = 5 * 2 * 1 * 100 * 4
+    want = (n + 255) // 256 * 256
+    assert lib.streamkl_fwd_workspace_size(1, 1, 100, 200, 64, 0, 16) == want
+
+
+def _fwd(lib, q=0x1000, NQ=8, NK=8, d=64, causal=0, kl=0x2000, status=0x3000, scale=0.125):
+    P = ctypes.c_void_p
+    return lib.streamkl_fwd(P(q), P(q), P(q), P(q), 1, 1, NQ, NK, d, scale, causal, 0, P(kl),
+                            P(kl), P(kl), None, 0, P(status), None)
+
+
+def test_argument_validation_is_synchronous(lib):
+    assert _fwd(lib, q=0) == 1  # NULL input
+    assert b"q1" in lib.streamkl_last_error()
+    assert _fwd(lib, q=0x1001) == 1  # misaligned
+    assert _fwd(lib, d=96) == 2  # unsupported head dim
+    assert _fwd(lib, NQ=16, NK=8, causal=1) == 1  # causal needs NQ <= NK
+    assert _fwd(lib, kl=0) == 1
+    assert _fwd(lib, status=0) == 1
+    assert _fwd(lib, scale=0.0) == 1
+    assert _fwd(lib, NQ=0) == 1
+
+
+def test_backward_validation(lib):
+    P = ctypes.c_void_p
+    a = P(0x1000)
+
+    def bwd(dq1, dk1, ws=0x4000, ws_bytes=1 << 20):
+        return lib.streamkl_bwd(a, a, a, a, 1, 1, 8, 8, 64, 0.125, 0, a, a, a, a, a, a,
+                                P(dq1) if dq1 else None, P(dk1) if dk1 else None,
+                                P(ws) if ws else None, ws_bytes, a, None)
+
+    assert bwd(0x1000, 0) == 1  # dq1 without dk1
+    assert bwd(0, 0x1000) == 1
+    assert bwd(0, 0, ws=0) == 1  # no workspace
+    assert bwd(0, 0, ws_bytes=16) == 1  # workspace too small
+    assert b"workspace" in lib.streamkl_last_error()
+
+
+def test_selftest_validation(lib):
+    assert lib.streamkl_selftest_wait_timeout(None, 100, None) == 1
+    assert lib.streamkl_selftest_wait_timeout(ctypes.c_void_p(0x1000), 0, None) == 1
+
+
+def test_pair_counts():
+    from attention_kl_loss_gb300 import synthetic
+    w = synthetic.WORKLOADS["causal64k"]
+    assert w.live_pairs_per_head() == 65536 * 65537 // 2
+    w4 = synthetic.WORKLOADS["splitk"]
+    brute = sum(i + 1 + (131072 - 512) for i in range(512))
+    assert w4.live_pairs_per_head() == brute

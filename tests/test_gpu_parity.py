@@ -1,0 +1,209 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle.
+
+Tolerances (fixed for the whole suite):
+  KL per row   |gpu - ref| <= 2e-3 + 1e-2 |ref|
+  lse1, lse2   relative L2 error <= 1e-4
+  gradients    relative L2 error <= 1e-2 per tensor
+Small and ragged shapes are compared element by element in full; the named
+workloads run at full size on the GPU and are checked on sampled heads, rows
+and keys that the oracle computes exactly (heads and rows are independent),
+plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+from attention_kl_loss_gb300 import binding, synthetic
+from oracle import streamkl_oracle as orc
+
+pytestmark = pytest.mark.gpu
+
+KL_ABS, KL_REL, LSE_REL, GRAD_REL = 2e-3, 1e-2, 1e-4, 1e-2
+
+
+def rel_l2(got, ref):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def assert_kl(got, ref):
+    err = np.abs(np.asarray(got, np.float64) - ref)
+    bound = KL_ABS + KL_REL * np.abs(ref)
+    worst = int(np.argmax(err - bound))
+    assert np.all(err <= bound), f"KL mismatch at {worst}: got {np.ravel(got)[worst]} ref {np.ravel(ref)[worst]}"
+
+
+def assert_grad(got, ref, name):
+    e = rel_l2(got, ref)
+    assert e <= GRAD_REL, f"{name}: rel L2 {e:.3e}"
+
+
+def host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run(w, seed=0, grad1=None, splits=0, inputs=None):
+    grad1 = w.grad1 if grad1 is None else grad1
+    dev = torch.device("cuda")
+    q1, k1, q2, k2, g = inputs if inputs is not None else synthetic.make_inputs(w, seed, dev)
+    status = binding.new_status(dev)
+    kl, lse1, lse2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, num_splits=splits,
+                                          dev_status=status)
+    grads = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                 grad1=grad1, dev_status=status)
+    binding.raise_on_device_status(status, w.name)
+    return (q1, k1, q2, k2, g), (kl, lse1, lse2), grads
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_lib):
+    return cuda_lib
+
+
+def test_bounded_wait_times_out_cleanly():
+    st = binding.selftest_wait_timeout(20000)
+    torch.cuda.synchronize()
+    assert int(st.item()) == binding.STREAMKL_ERR_TIMEOUT
+    # the context is still usable afterwards
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum().item()) == 4.0
+
+
+def full_check(w, seed=0, grad1=True, splits=0):
+    ins, (kl, l1, l2), grads = run(w, seed, grad1, splits)
+    h = [host(t) for t in ins[:4]]
+    okl, ol1, ol2 = orc.forward(*h, w.scale, w.causal)
+    assert_kl(kl.cpu().numpy(), okl)
+    assert rel_l2(l1.cpu().numpy(), ol1) <= LSE_REL
+    assert rel_l2(l2.cpu().numpy(), ol2) <= LSE_REL
+    og = orc.backward(*h, w.scale, w.causal, ins[4].cpu().numpy(), grad1)
+    names = ["dq2", "dk2", "dq1", "dk1"]
+    for i in range(4 if grad1 else 2):
+        assert_grad(host(grads[i]), og[i], names[i])
+    if not grad1:
+        assert grads[2] is None and grads[3] is None
+
+
+def test_tiny_workload_forward_and_backward():
+    full_check(synthetic.WORKLOADS["tiny"], seed=0, grad1=False)
+
+
+def test_tiny_workload_both_gradient_sets():
+    full_check(synthetic.WORKLOADS["tiny"], seed=1, grad1=True)
+
+
+RAGGED = [
+    (1, 1, 64, False), (1, 300, 128, True), (129, 129, 64, True), (200, 333, 128, True),
+    (333, 200, 64, False), (77, 1000, 128, False), (256, 384, 128, True), (130, 131, 64, True),
+]
+
+
+@pytest.mark.parametrize("NQ,NK,d,causal", RAGGED)
+def test_ragged_shapes(NQ, NK, d, causal):
+    w = synthetic.custom(f"ragged{NQ}x{NK}d{d}", B=2, H=3, NQ=NQ, NK=NK, d=d, causal=causal,
+                         noise=0.5, grad1=True)
+    full_check(w, seed=NQ + NK)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_peaked_teacher_independent_student(d):
+    w = synthetic.custom("peaked", B=1, H=2, NQ=384, NK=640, d=d, causal=False, teacher_std=3.0,
+                         student="independent", grad1=True)
+    full_check(w, seed=5)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_identical_inputs_give_exact_zero(causal):
+    w = synthetic.custom("same", B=1, H=2, NQ=256, NK=384, d=128, causal=causal, noise=0.0,
+                         grad1=True)
+    q1, k1, _, _, g = synthetic.make_inputs(w, 3, torch.device("cuda"))
+    _, (kl, l1, l2), grads = run(w, inputs=(q1, k1, q1, k1, g))
+    assert torch.all(kl == 0)
+    assert torch.equal(l1, l2)
+    for t in grads:
+        assert torch.all(t == 0)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 8])
+def test_split_invariance(splits):
+    """Forced key splits give the oracle's answer (and each other's)."""
+    w = synthetic.custom("split", B=1, H=4, NQ=256, NK=2048 + 77, d=128, causal=True, noise=0.2)
+    ins, (kl, l1, l2), _ = run(w, seed=9, grad1=False, splits=splits)
+    h = [host(t) for t in ins[:4]]
+    okl, ol1, ol2 = orc.forward(*h, w.scale, w.causal)
+    assert_kl(kl.cpu().numpy(), okl)
+    assert rel_l2(l1.cpu().numpy(), ol1) <= LSE_REL
+    ref_kl, _, _ = binding.streamkl_fwd(*ins[:4], w.scale, w.causal, num_splits=1)
+    assert torch.allclose(kl, ref_kl, rtol=1e-4, atol=1e-5)
+
+
+def sampled_check(w, heads, rows, key_sets, seed=0):
+    """Full-size GPU run; oracle on sampled heads/rows/keys.
+
+    rows: query rows whose KL, lse and dQ are compared.
+    key_sets: key index arrays whose dK is compared; the oracle sums over every
+    query row that can see them.
+    """
+    ins, (kl, l1, l2), grads = run(w, seed)
+    g_all = ins[4]
+    n_sets = 4 if w.grad1 else 2
+    for (b, hh) in heads:
+        h = [host(t[b, hh]) for t in ins[:4]]
+        g = g_all[b, hh].cpu().numpy().astype(np.float64)
+        okl, ol1, ol2 = orc.head_forward(*h, w.scale, w.causal, rows=rows)
+        assert_kl(kl[b, hh].cpu().numpy()[rows], okl)
+        assert rel_l2(l1[b, hh].cpu().numpy()[rows], ol1) <= LSE_REL
+        assert rel_l2(l2[b, hh].cpu().numpy()[rows], ol2) <= LSE_REL
+        og = orc.head_backward(*h, w.scale, w.causal, g, w.grad1, rows=rows)
+        assert_grad(host(grads[0][b, hh])[rows], og[0], "dq2")
+        if w.grad1:
+            assert_grad(host(grads[2][b, hh])[rows], og[2], "dq1")
+        for keys in key_sets:
+            lo = int(keys.min())
+            # rows that can see key lo: i + off >= lo
+            first = max(0, lo - (w.NK - w.NQ)) if w.causal else 0
+            rr = np.arange(first, w.NQ)
+            ogk = orc.head_backward(*h, w.scale, w.causal, g, w.grad1, rows=rr)
+            assert_grad(host(grads[1][b, hh])[keys], ogk[1][keys], "dk2")
+            if w.grad1:
+                assert_grad(host(grads[3][b, hh])[keys], ogk[3][keys], "dk1")
+    # any size: shift invariance makes every head's dK sum to zero over keys
+    for i in (1, 3)[: n_sets // 2]:
+        dk = grads[i].float()
+        s = dk.sum(dim=2).norm() / dk.norm(dim=-1).sum(dim=2).norm()
+        assert float(s) < 2e-2, f"sum_j dK[j] not ~0 ({float(s):.3e})"
+    for t in (kl, l1, l2):
+        assert torch.isfinite(t).all()
+    for t in grads[:n_sets]:
+        assert torch.isfinite(t.float()).all()
+
+
+def _rows(n, k, seed):
+    rng = np.random.default_rng(seed)
+    r = np.unique(np.concatenate([[0, 1, n - 1], rng.choice(n, size=min(n, k), replace=False)]))
+    return r
+
+
+def test_mid_workload_full_size():
+    w = synthetic.WORKLOADS["mid"]
+    sampled_check(w, heads=[(0, 0), (1, 15)], rows=_rows(w.NQ, 384, 1),
+                  key_sets=[np.arange(0, 128), np.arange(w.NK - 200, w.NK)])
+
+
+def test_stress_workload_full_size():
+    w = synthetic.WORKLOADS["stress"]
+    sampled_check(w, heads=[(0, 3)], rows=_rows(w.NQ, 256, 2),
+                  key_sets=[np.arange(w.NK - 128, w.NK)])
+
+
+def test_splitk_workload_full_size():
+    w = synthetic.WORKLOADS["splitk"]
+    sampled_check(w, heads=[(0, 0), (3, 31)], rows=np.arange(w.NQ),
+                  key_sets=[np.arange(0, 64), np.arange(w.NK - 600, w.NK)])
+
+
+def test_causal64k_workload_full_size():
+    w = synthetic.WORKLOADS["causal64k"]
+    sampled_check(w, heads=[(0, 0), (0, 31)], rows=_rows(w.NQ, 256, 3),
+                  key_sets=[np.arange(w.NK - 256, w.NK)])
