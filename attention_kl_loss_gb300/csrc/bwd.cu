@@ -54,6 +54,7 @@ struct BwdLayout {
   static constexpr int ALLOC = BYTES + 1024;
   // TMEM columns
   static constexpr bool ALIAS = (D == 128 && GRAD1);  // dQ reuses S columns
+  static constexpr bool DQT = (D == 128);  // dQ held transposed (lanes = d)
   static constexpr uint32_t COL_S1 = 0, COL_S2 = 128;
   static constexpr uint32_t COL_DK2 = 256;
   static constexpr uint32_t COL_DK1 = 256 + D;
@@ -174,6 +175,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_s = idesc_bf16(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t id_dk = idesc_bf16(kBlockN, D, 1, 1);
       constexpr uint32_t id_dq = idesc_bf16(kBlockM, D, 0, 1);
+      constexpr uint32_t id_dqt = idesc_bf16(D, kBlockM, 1, 0);
       bool ok = wait_bounded(k_full, 0, wc);
       for (int it = 0; ok && it < n_iter; ++it) {
         const int s = it % L::QSTAGES;
@@ -199,38 +201,42 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mma_commit(s_full);
         if (!wait_bounded(ds_full, par, wc)) break;
-        if (!L::ALIAS && !wait_bounded(dq_free, par ^ 1, wc)) break;
         tc_fence_after();
-        // 8 k-steps of 16 over the tile's 128 query rows (dK) or 128 keys (dQ)
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          // dK2 += dS2^T Q2: A = dS2 viewed MN-major (keys contiguous),
-          // B = Q2 MN-major (d contiguous); K index = query row.
-          mma_bf16(tmem + L::COL_DK2, smem_desc_sw128(sb + L::OFF_DS2 + k * 2048, 16384, 1024),
-                   smem_desc_sw128(q2s + k * 2048, 16384, 1024), id_dk, (it > 0 || k > 0));
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          // dQ2 = dS2 K2: A = dS2 K-major (keys contiguous), B = K2 MN-major.
-          const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_bf16(tmem + L::COL_DQ2, smem_desc_sw128(sb + L::OFF_DS2 + koff, 16, 1024),
-                   smem_desc_sw128(sb + L::OFF_K2 + k * 2048, 16384, 1024), id_dq, k > 0);
-        }
-        if (GRAD1) {
+        // dK_t += dS_t^T Q_t, 8 k-steps over the tile's 128 query rows:
+        // A = dS_t viewed MN-major (keys contiguous), B = Q_t MN-major (d contiguous).
+        auto mma_dk = [&](uint32_t col, uint32_t ds, uint32_t qs) {
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_bf16(tmem + L::COL_DK1, smem_desc_sw128(sb + L::OFF_DS1 + k * 2048, 16384, 1024),
-                     smem_desc_sw128(q1s + k * 2048, 16384, 1024), id_dk, (it > 0 || k > 0));
+            mma_bf16(tmem + col, smem_desc_sw128(ds + k * 2048, 16384, 1024),
+                     smem_desc_sw128(qs + k * 2048, 16384, 1024), id_dk, (it > 0 || k > 0));
+        };
+        mma_dk(L::COL_DK2, sb + L::OFF_DS2, q2s);
+        if (GRAD1) mma_dk(L::COL_DK1, sb + L::OFF_DS1, q1s);
+        mma_commit(q_empty(s));  // the Q tile is no longer read: start the next load
+        if (!L::ALIAS && !wait_bounded(dq_free, par ^ 1, wc)) break;
+        tc_fence_after();
+        // dQ, 8 k-steps over the tile's 128 keys.
+        //  d == 128: dQ_t^T = K_t^T dS_t^T (M = d, N = query rows; A = K_t MN-major,
+        //            B = dS_t K-major): a TMEM lane then holds one d column, so
+        //            the readout reduces whole 128-byte row segments at once.
+        //  d == 64:  dQ_t = dS_t K_t (M = query rows, N = d; A = dS_t K-major,
+        //            B = K_t MN-major).
+        auto mma_dq = [&](uint32_t col, uint32_t ds, uint32_t ks) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
-            mma_bf16(tmem + L::COL_DQ1, smem_desc_sw128(sb + L::OFF_DS1 + koff, 16, 1024),
-                     smem_desc_sw128(sb + L::OFF_K1 + k * 2048, 16384, 1024), id_dq, k > 0);
+            if (L::DQT)
+              mma_bf16(tmem + col, smem_desc_sw128(ks + k * 2048, 16384, 1024),
+                       smem_desc_sw128(ds + koff, 16, 1024), id_dqt, k > 0);
+            else
+              mma_bf16(tmem + col, smem_desc_sw128(ds + koff, 16, 1024),
+                       smem_desc_sw128(ks + k * 2048, 16384, 1024), id_dq, k > 0);
           }
-        }
+        };
+        mma_dq(L::COL_DQ2, sb + L::OFF_DS2, sb + L::OFF_K2);
+        if (GRAD1) mma_dq(L::COL_DQ1, sb + L::OFF_DS1, sb + L::OFF_K1);
         mma_commit(dq_full);
         mma_commit(ds_free);
-        mma_commit(q_empty(s));
       }
       mma_commit(dk_full);
       mma_commit(drain);
@@ -305,23 +311,41 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
-      // dQ readout: this thread's row, d columns [wg*D/2, (wg+1)*D/2)
+      // dQ readout and reduction into the fp32 accumulator
       if (!(ok = wait_bounded(dq_full, par, wc))) break;
       tc_fence_after();
 #pragma unroll
       for (int set = 0; set < (GRAD1 ? 2 : 1); ++set) {
-        const uint32_t col = (set == 0 ? L::COL_DQ2 : L::COL_DQ1) + wg * (D / 2);
         float* acc = (set == 0 ? dq2acc : dq1acc);
+        if (L::DQT) {
+          // lane = d column (32*quarter + lane); warpgroup w takes query rows
+          // [64w, 64w+64) of the tile; one red per row covers 128 contiguous bytes
+          const uint32_t col = (set == 0 ? L::COL_DQ2 : L::COL_DQ1) + wg * 64;
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          float v[32];
-          tmem_ld32(tmem + lane_off + col + h * 32, v);
-          tmem_wait_ld();
-          if (qrow < NQ) {
-            float* dst = acc + (static_cast<size_t>(bh) * NQ + qrow) * D + wg * (D / 2) + h * 32;
+          for (int h = 0; h < 2; ++h) {
+            float v[32];
+            tmem_ld32(tmem + lane_off + col + h * 32, v);
+            tmem_wait_ld();
+            const int row0 = (qb0 + it) * kBlockM + wg * 64 + h * 32;
+            float* dst = acc + (static_cast<size_t>(bh) * NQ + row0) * D + quarter * 32 + lane;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              red_add_v4(dst + 4 * j, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            for (int j = 0; j < 32; ++j)
+              if (row0 + j < NQ) red_add_f32(dst + static_cast<size_t>(j) * D, v[j]);
+          }
+        } else {
+          // lane = query row; this thread's d columns [wg*D/2, (wg+1)*D/2)
+          const uint32_t col = (set == 0 ? L::COL_DQ2 : L::COL_DQ1) + wg * (D / 2);
+#pragma unroll
+          for (int h = 0; h < D / 64; ++h) {
+            float v[32];
+            tmem_ld32(tmem + lane_off + col + h * 32, v);
+            tmem_wait_ld();
+            if (qrow < NQ) {
+              float* dst = acc + (static_cast<size_t>(bh) * NQ + qrow) * D + wg * (D / 2) + h * 32;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                red_add_v4(dst + 4 * j, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            }
           }
         }
       }

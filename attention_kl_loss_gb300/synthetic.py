@@ -65,6 +65,10 @@ WORKLOADS = {
         Workload("splitk", B=4, H=32, NQ=512, NK=131072, d=128, causal=True, noise=0.1),
         Workload("stress", B=1, H=8, NQ=16384, NK=16384, d=64, causal=False,
                  teacher_std=3.0, student="independent", student_std=1.0),
+        # smaller causal case with the 64K workload's tile mix, sized for
+        # profiler captures (256 MiB of inputs: above L2, a few GB at most)
+        Workload("causal16k_profile", B=1, H=16, NQ=16384, NK=16384, d=128, causal=True,
+                 noise=0.2, grad1=True),
     ]
 }
 
