@@ -41,6 +41,8 @@ _SIGNATURES = {
     "streamkl_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _P,
                           _P, _P, _P, _Z, _P, _P]),
     "streamkl_selftest_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
+    "streamkl_fwd_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P,
+                                  _P, _P]),
 }
 
 
@@ -151,6 +153,26 @@ def streamkl_fwd(q1, k1, q2, k2, scale: Optional[float] = None, causal: bool = F
                           _ptr(ws), need if ws is not None else 0, _ptr(status),
                           _stream_handle(stream))
     _check(st, "streamkl_fwd")
+    return kl, lse1, lse2
+
+
+def streamkl_fwd_noalloc(q1, k1, q2, k2, out, scale: Optional[float] = None,
+                         causal: bool = False, num_splits: int = 0, dev_status=None, stream=None):
+    """Forward pass through the library's allocation-free entry point.
+
+    For callers that cannot allocate device memory: the outputs ``out`` =
+    (kl, lse1, lse2) must be given, and the split scratch is the library's
+    built-in 16 MiB array (shared by every call on the device)."""
+    lib = load()
+    B, H, NQ, NK, d = _dims(q1, k1, q2, k2)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    kl, lse1, lse2 = out
+    if dev_status is None:
+        raise ValueError("dev_status must be given (this path allocates nothing)")
+    st = lib.streamkl_fwd_noalloc(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), B, H, NQ, NK, d, scale,
+                                  int(causal), int(num_splits), _ptr(kl), _ptr(lse1), _ptr(lse2),
+                                  _ptr(dev_status), _stream_handle(stream))
+    _check(st, "streamkl_fwd_noalloc")
     return kl, lse1, lse2
 
 

@@ -13,7 +13,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "../../include/streamkl.h"
+#include "streamkl.h"
 #include "kernels.h"
 
 namespace {
@@ -258,6 +258,71 @@ streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, con
     if (e != cudaSuccess) return cuda_fail(e, "split combine launch");
   }
   return STREAMKL_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Forward pass without any caller-provided workspace.
+//
+// Split partial states go to a fixed scratch array compiled into the library
+// instead of a buffer the caller allocates. Every GPU that loads the library
+// holds this array until the process exits, and every call on that GPU shares
+// it, so calls whose kernels overlap on the GPU (other streams, other host
+// threads) race on it. Nothing in it has to start at zero: each call writes
+// every partial state it later reads.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace {
+
+constexpr size_t kFwdScratchBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_fwd_scratch[kFwdScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_dev_ptr[256] = {};  // device address of g_fwd_scratch, per device
+
+// Device address of the scratch array on the current device. The host-side
+// name of the array is only a stand-in, so the address is looked up once per
+// device (with that device current) and cached.
+streamkl_status fwd_scratch_ptr(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 256) return fail(STREAMKL_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_dev_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_fwd_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    g_scratch_dev_ptr[dev] = p;
+  }
+  *out = g_scratch_dev_ptr[dev];
+  return STREAMKL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+streamkl_status streamkl_fwd_noalloc(const void* q1, const void* k1, const void* q2,
+                                     const void* k2, int B, int H, int NQ, int NK, int d,
+                                     float scale, int causal, int num_splits, float* kl,
+                                     float* lse1, float* lse2, int* dev_status, void* stream) {
+  g_err[0] = '\0';
+  streamkl_status st = check_sizes(B, H, NQ, NK, d, causal);
+  if (st != STREAMKL_OK) return st;
+  if (num_splits < 0) return fail(STREAMKL_ERR_INVALID_ARG, "num_splits must be >= 0");
+  int splits, tps;
+  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK), NK, &splits, &tps);
+  const size_t need = fwd_ws(B, H, NQ, splits);
+  if (need > kFwdScratchBytes)
+    return fail(STREAMKL_ERR_INVALID_ARG,
+                "this call needs %zu bytes of split scratch but the built-in scratch holds %zu; "
+                "request fewer splits or use streamkl_fwd with a workspace",
+                need, kFwdScratchBytes);
+  void* scratch = nullptr;
+  if (need > 0 && (st = fwd_scratch_ptr(&scratch)) != STREAMKL_OK) return st;
+  return streamkl_fwd(q1, k1, q2, k2, B, H, NQ, NK, d, scale, causal, splits, kl, lse1, lse2,
+                      scratch, need > 0 ? kFwdScratchBytes : 0, dev_status, stream);
 }
 
 streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2, int B,

@@ -98,6 +98,36 @@ streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, con
                              void* workspace, size_t ws_bytes, int* dev_status, void* stream);
 
 /*
+ * Forward pass that allocates nothing and takes no workspace. The paper has
+ * no counterpart; this entry point exists for callers that only hold the
+ * input and output buffers handed to them and cannot obtain device memory of
+ * their own: a plug-in operator inside another runtime that offers no
+ * workspace, or code whose device memory is owned by a host framework's pool,
+ * where a cudaMalloc would fail, fragment that pool or stall the device.
+ *
+ * Same arguments, results and errors as streamkl_fwd, minus the workspace.
+ * The split partial states go to a scratch array built into the library:
+ * 16 MiB (16777216 bytes) of device memory that every GPU which loads the
+ * library keeps until the process exits. A call whose split plan needs more
+ * than that (5 floats per split, batch, head and query row, rounded up to 256
+ * bytes; see streamkl_fwd_workspace_size) returns STREAMKL_ERR_INVALID_ARG
+ * with the sizes in streamkl_last_error(); pass fewer splits or use
+ * streamkl_fwd. Calls without splits do not touch the scratch.
+ *
+ * The first call that uses the scratch on a device looks up its device
+ * address (with that device current) and caches it; make that first call
+ * before any stream capture. All calls on a device share the one array and
+ * each leaves its partial states in it; nothing there needs clearing because
+ * every call writes all the states it reads, but calls whose kernels may
+ * overlap on the GPU (different streams, other host threads) race on it and
+ * must be ordered by the caller.
+ */
+streamkl_status streamkl_fwd_noalloc(const void* q1, const void* k1, const void* q2,
+                                     const void* k2, int B, int H, int NQ, int NK, int d,
+                                     float scale, int causal, int num_splits, float* kl,
+                                     float* lse1, float* lse2, int* dev_status, void* stream);
+
+/*
  * Backward pass of L = sum_{b,h,i} dkl[b,h,i] * KL[b,h,i] (gist.science
  * technical summary, section 2: probabilities regenerated tile by tile as
  * P_t = exp(S_t - LSE_t); "Configuracion 1": P1 fixed, gradients to Q2, K2;

@@ -1,0 +1,80 @@
+"""The allocation-free forward entry point, streamkl_fwd_noalloc.
+
+Some callers cannot allocate device memory: a plug-in operator running inside
+another runtime that hands it only its input and output buffers, or code whose
+device memory belongs to a host framework's pool, where an extra cudaMalloc
+would fail, fragment the pool or stall the device. For them the library keeps
+the forward pass's split scratch in a device array compiled into it. These
+checks call that entry point through the C ABI and hold its results to the
+regular streamkl_fwd (which takes a caller-provided workspace), with the
+suite's tolerances, on two calls in a row that use the shared scratch with
+different shapes. The file sorts last so that a run stopping at the first
+failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from attention_kl_loss_gb300 import binding, synthetic
+
+KL_ABS, KL_REL, LSE_REL = 2e-3, 1e-2, 1e-4
+SCRATCH_BYTES = 16 << 20
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_kl_loss_gb300 import build
+    build.build()
+    return binding.load()
+
+
+def test_rejects_split_plans_beyond_the_builtin_scratch(lib):
+    """Runs on the CPU: the size check comes before any device work."""
+    p = ctypes.c_void_p(0x1000)
+    # 8 splits x 32 heads x 65536 rows x 5 floats = 40 MiB > 16 MiB
+    st = lib.streamkl_fwd_noalloc(p, p, p, p, 1, 32, 65536, 65536, 128, 0.088, 1, 8, p, p, p, p,
+                                  None)
+    assert st == binding.STREAMKL_ERR_INVALID_ARG
+    msg = lib.streamkl_last_error()
+    assert str(SCRATCH_BYTES).encode() in msg and b"workspace" in msg
+
+
+def _close(got, ref):
+    err = (got.double() - ref.double()).abs()
+    bound = KL_ABS + KL_REL * ref.double().abs()
+    return bool((err <= bound).all())
+
+
+def _rel_l2(got, ref):
+    return float((got.double() - ref.double()).norm() / ref.double().norm())
+
+
+@pytest.mark.gpu
+def test_noalloc_forward_matches_workspace_forward_on_two_calls(lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda")
+    cases = [
+        (synthetic.custom("noalloc_a", B=2, H=4, NQ=384, NK=4096 + 77, d=128, causal=True,
+                          noise=0.2), 4, 11),
+        (synthetic.custom("noalloc_b", B=1, H=8, NQ=200, NK=3000, d=64, causal=False,
+                          teacher_std=2.0, noise=0.5), 3, 12),
+    ]
+    for w, splits, seed in cases:
+        assert binding.streamkl_fwd_workspace_size(w.B, w.H, w.NQ, w.NK, w.d, w.causal,
+                                                   splits) > 0  # the scratch is really used
+        q1, k1, q2, k2, _ = synthetic.make_inputs(w, seed, dev)
+        ref = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, num_splits=splits)
+        out = tuple(torch.full((w.B, w.H, w.NQ), float("nan"), device=dev) for _ in range(3))
+        status = binding.new_status(dev)
+        binding.streamkl_fwd_noalloc(q1, k1, q2, k2, out, w.scale, w.causal, num_splits=splits,
+                                     dev_status=status)
+        binding.raise_on_device_status(status, "streamkl_fwd_noalloc")
+        kl, lse1, lse2 = out
+        assert torch.isfinite(kl).all()
+        assert _close(kl, ref[0]), w.name
+        assert _rel_l2(lse1, ref[1]) <= LSE_REL
+        assert _rel_l2(lse2, ref[2]) <= LSE_REL
+    assert np.isfinite(float(kl.sum()))
