@@ -6,15 +6,20 @@ The computation lives in the CUDA library built from ``csrc/`` (C ABI in
 ``include/streamkl.h``); this package only marshals arguments to it.
 """
 from .binding import (  # noqa: F401
+    BWD_FUSED,
+    BWD_SEPARATE,
     StreamKLError,
+    bwd_algorithm,
     choose_splits,
     load,
     new_status,
     raise_on_device_status,
     selftest_wait_timeout,
+    set_bwd_algorithm,
     streamkl_bwd,
     streamkl_bwd_workspace_size,
     streamkl_fwd,
+    streamkl_fwd_noalloc,
     streamkl_fwd_workspace_size,
     streamkl_workspace_size,
 )

@@ -41,6 +41,8 @@ _SIGNATURES = {
     "streamkl_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _P,
                           _P, _P, _P, _Z, _P, _P]),
     "streamkl_selftest_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
+    "streamkl_bwd_algorithm": (_I, [_I, _I, _I, _I, _I, _I, _I]),
+    "streamkl_set_bwd_algorithm": (_I, [_I]),
     "streamkl_fwd_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P,
                                   _P, _P]),
 }
@@ -118,6 +120,22 @@ def streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal, want_grad1) -> int:
 
 def streamkl_workspace_size(B, H, NQ, NK, d, causal, want_grad1) -> int:
     return int(load().streamkl_workspace_size(B, H, NQ, NK, d, int(causal), int(want_grad1)))
+
+
+BWD_SEPARATE = 0
+BWD_FUSED = 1
+
+
+def bwd_algorithm(B, H, NQ, NK, d, causal, want_grad1=False) -> int:
+    """0 = separate dK/dQ kernels, 1 = fused kernel with dQ atomics."""
+    return int(load().streamkl_bwd_algorithm(B, H, NQ, NK, d, int(causal), int(want_grad1)))
+
+
+def set_bwd_algorithm(algo: Optional[int]) -> None:
+    """Force the backward algorithm process-wide (None = automatic)."""
+    v = -1 if algo is None else int(algo)
+    if load().streamkl_set_bwd_algorithm(v) != 0:
+        raise ValueError(f"invalid backward algorithm {algo!r}")
 
 
 def new_status(device=None) -> torch.Tensor:

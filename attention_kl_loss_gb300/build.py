@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "libstreamkl.so"
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_sep.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]

@@ -11,6 +11,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "streamkl.h"
@@ -126,6 +127,32 @@ void split_plan(int requested, int NK, int* splits, int* tps) {
   *splits = (tiles + per - 1) / per;
 }
 
+// Backward algorithm: 0 = separate dK and dQ kernels (accumulators stay on
+// chip, no atomics, no workspace), 1 = one fused kernel per key tile with dQ
+// reduced through fp32 atomics. STREAMKL_BWD_ALGO=separate|fused sets the
+// initial override; streamkl_set_bwd_algorithm changes it.
+std::atomic<int> g_forced_algo{-2};  // -2: environment not read yet, -1: automatic
+
+int forced_algo() {
+  int v = g_forced_algo.load();
+  if (v == -2) {
+    const char* s = std::getenv("STREAMKL_BWD_ALGO");
+    int e = -1;
+    if (s && s[0] == 'f') e = 1;
+    if (s && s[0] == 's') e = 0;
+    g_forced_algo.compare_exchange_strong(v, e);
+    v = g_forced_algo.load();
+  }
+  return v;
+}
+
+int bwd_algo_impl(int B, int H, int NQ, int NK) {
+  const int forced = forced_algo();
+  if (forced >= 0) return forced;
+  (void)B, (void)H, (void)NQ, (void)NK;
+  return 0;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 size_t fwd_ws(int B, int H, int NQ, int splits) {
@@ -133,7 +160,8 @@ size_t fwd_ws(int B, int H, int NQ, int splits) {
   return align256(static_cast<size_t>(5) * splits * B * H * NQ * sizeof(float));
 }
 
-size_t bwd_ws(int B, int H, int NQ, int d, int grad1) {
+size_t bwd_ws(int B, int H, int NQ, int NK, int d, int grad1) {
+  if (bwd_algo_impl(B, H, NQ, NK) == 0) return 0;
   const size_t one = align256(static_cast<size_t>(B) * H * NQ * d * sizeof(float));
   return grad1 ? 2 * one : one;
 }
@@ -197,7 +225,23 @@ size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int caus
 
 size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
   if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return 0;
-  return bwd_ws(B, H, NQ, d, want_grad1 ? 1 : 0);
+  return bwd_ws(B, H, NQ, NK, d, want_grad1 ? 1 : 0);
+}
+
+int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
+  (void)want_grad1;
+  if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return -1;
+  return bwd_algo_impl(B, H, NQ, NK);
+}
+
+int streamkl_set_bwd_algorithm(int algo) {
+  if (algo < -1 || algo > 1) {
+    fail(STREAMKL_ERR_INVALID_ARG, "algorithm must be -1, 0 or 1");
+    return -1;
+  }
+  forced_algo();  // settle the environment's initial value first
+  g_forced_algo.store(algo);
+  return 0;
 }
 
 size_t streamkl_workspace_size(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
@@ -343,8 +387,9 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   if (!dev_status) return fail(STREAMKL_ERR_INVALID_ARG, "dev_status must be non-NULL");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(STREAMKL_ERR_INVALID_ARG, "scale must be finite and > 0");
   const int grad1 = dq1 != nullptr;
-  const size_t need = bwd_ws(B, H, NQ, d, grad1);
-  if (!workspace || ws_bytes < need || !aligned16(workspace))
+  const int algo = bwd_algo_impl(B, H, NQ, NK);
+  const size_t need = bwd_ws(B, H, NQ, NK, d, grad1);
+  if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
     return fail(STREAMKL_ERR_INVALID_ARG, "backward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
 
   const int BH = B * H;
@@ -355,6 +400,33 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   if ((st = make_map(&mk2, k2, BH, NK, d, "k2")) != STREAMKL_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (algo == 0) {
+    skl::BwdSepArgs a{};
+    a.tm_q1 = &mq1;
+    a.tm_k1 = &mk1;
+    a.tm_q2 = &mq2;
+    a.tm_k2 = &mk2;
+    a.BH = BH;
+    a.NQ = NQ;
+    a.NK = NK;
+    a.d = d;
+    a.causal = causal;
+    a.grad1 = grad1;
+    a.scale = scale;
+    a.kl = kl;
+    a.lse1 = lse1;
+    a.lse2 = lse2;
+    a.g = dkl;
+    a.dq2 = dq2;
+    a.dk2 = dk2;
+    a.dq1 = dq1;
+    a.dk1 = dk1;
+    a.dev_status = dev_status;
+    a.timeout_ns = wait_timeout_ns();
+    cudaError_t e = skl::launch_bwd_separate(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return STREAMKL_OK;
+  }
   cudaError_t e = cudaMemsetAsync(workspace, 0, need, s);
   if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
   const size_t one = need / (grad1 ? 2 : 1);

@@ -186,16 +186,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         const uint32_t q1s = sb + L::OFF_Q + s * 2 * L::TILE;
         const uint32_t q2s = q1s + L::TILE;
-        // S_t = Q_t K_t^T, both operands K-major (d contiguous)
+        // S_t = Q_t K_t^T, both operands K-major (d contiguous); the two GEMMs'
+        // k-steps interleaved so that independent accumulators overlap
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
           mma_bf16(tmem + L::COL_S1, smem_desc_sw128(q1s + koff, 16, 1024),
                    smem_desc_sw128(sb + L::OFF_K1 + koff, 16, 1024), id_s, k > 0);
-        }
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
           mma_bf16(tmem + L::COL_S2, smem_desc_sw128(q2s + koff, 16, 1024),
                    smem_desc_sw128(sb + L::OFF_K2 + koff, 16, 1024), id_s, k > 0);
         }
@@ -204,14 +201,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tc_fence_after();
         // dK_t += dS_t^T Q_t, 8 k-steps over the tile's 128 query rows:
         // A = dS_t viewed MN-major (keys contiguous), B = Q_t MN-major (d contiguous).
-        auto mma_dk = [&](uint32_t col, uint32_t ds, uint32_t qs) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            mma_bf16(tmem + col, smem_desc_sw128(ds + k * 2048, 16384, 1024),
-                     smem_desc_sw128(qs + k * 2048, 16384, 1024), id_dk, (it > 0 || k > 0));
-        };
-        mma_dk(L::COL_DK2, sb + L::OFF_DS2, q2s);
-        if (GRAD1) mma_dk(L::COL_DK1, sb + L::OFF_DS1, q1s);
+        for (int k = 0; k < 8; ++k) {
+          mma_bf16(tmem + L::COL_DK2, smem_desc_sw128(sb + L::OFF_DS2 + k * 2048, 16384, 1024),
+                   smem_desc_sw128(q2s + k * 2048, 16384, 1024), id_dk, (it > 0 || k > 0));
+          if (GRAD1)
+            mma_bf16(tmem + L::COL_DK1, smem_desc_sw128(sb + L::OFF_DS1 + k * 2048, 16384, 1024),
+                     smem_desc_sw128(q1s + k * 2048, 16384, 1024), id_dk, (it > 0 || k > 0));
+        }
         mma_commit(q_empty(s));  // the Q tile is no longer read: start the next load
         if (!L::ALIAS && !wait_bounded(dq_free, par ^ 1, wc)) break;
         tc_fence_after();
@@ -221,20 +218,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         //            the readout reduces whole 128-byte row segments at once.
         //  d == 64:  dQ_t = dS_t K_t (M = query rows, N = d; A = dS_t K-major,
         //            B = K_t MN-major).
-        auto mma_dq = [&](uint32_t col, uint32_t ds, uint32_t ks) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
-            if (L::DQT)
-              mma_bf16(tmem + col, smem_desc_sw128(ks + k * 2048, 16384, 1024),
-                       smem_desc_sw128(ds + koff, 16, 1024), id_dqt, k > 0);
-            else
-              mma_bf16(tmem + col, smem_desc_sw128(ds + koff, 16, 1024),
-                       smem_desc_sw128(ks + k * 2048, 16384, 1024), id_dq, k > 0);
-          }
+        auto mma_dq = [&](uint32_t col, uint32_t ds, uint32_t ks, int k) {
+          const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
+          if (L::DQT)
+            mma_bf16(tmem + col, smem_desc_sw128(ks + k * 2048, 16384, 1024),
+                     smem_desc_sw128(ds + koff, 16, 1024), id_dqt, k > 0);
+          else
+            mma_bf16(tmem + col, smem_desc_sw128(ds + koff, 16, 1024),
+                     smem_desc_sw128(ks + k * 2048, 16384, 1024), id_dq, k > 0);
         };
-        mma_dq(L::COL_DQ2, sb + L::OFF_DS2, sb + L::OFF_K2);
-        if (GRAD1) mma_dq(L::COL_DQ1, sb + L::OFF_DS1, sb + L::OFF_K1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          mma_dq(L::COL_DQ2, sb + L::OFF_DS2, sb + L::OFF_K2, k);
+          if (GRAD1) mma_dq(L::COL_DQ1, sb + L::OFF_DS1, sb + L::OFF_K1, k);
+        }
         mma_commit(dq_full);
         mma_commit(ds_free);
       }

@@ -8,14 +8,16 @@
 // and read back by the softmax warps. Key tiles past a row block's causal
 // frontier are never loaded (same section: masked tiles are skipped).
 //
-// CTA layout (384 threads, one CTA per SM because of shared memory):
+// CTA layout (576 threads, one CTA per SM because of shared memory):
 //   warp 0       TMA producer: Q1/Q2 tile once, K1/K2 tiles through a ring
 //   warp 1       TMEM owner + MMA issuer: S1 = Q1 K1^T, S2 = Q2 K2^T per tile,
 //                double-buffered in TMEM (2 x 256 columns)
-//   warps 4..11  two softmax warpgroups; thread = one query row (TMEM lane);
-//                warpgroup w owns key columns [64w, 64w+64) of every tile and
-//                keeps its own five-scalar state; the two states are merged
-//                at the end exactly like split-K partials.
+//   warps 2..17  four softmax warpgroups; thread = one query row (TMEM lane
+//                of its warp's quarter); group g owns key columns
+//                [32g, 32g+32) of every tile and keeps its own five-scalar
+//                state; the four states are merged at the end exactly like
+//                split-K partials. Four warps per scheduler hide the exp2/FMA
+//                latency, and column pairs use the packed f32x2 FMA path.
 //
 // Numerics: exponentials are base 2 with the reference maximum kept in log2
 // units (r = m * scale * log2 e). The reference is only moved when a chunk's
@@ -28,7 +30,8 @@ namespace skl {
 
 namespace {
 
-constexpr int kFwdThreads = 384;
+constexpr int kFwdThreads = 576;  // 18 warps
+constexpr int kGroups = 4;        // softmax column groups (warpgroups)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTau = 8.0f;
@@ -45,8 +48,8 @@ struct FwdLayout {
   // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], s_empty[2], drain
   static constexpr int NBAR = 1 + 2 * STAGES + 4 + 1;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
-  static constexpr int OFF_XCH = OFF_MISC + 16;        // [5][128] floats
-  static constexpr int BYTES = OFF_XCH + 5 * kBlockM * 4;
+  static constexpr int OFF_XCH = OFF_MISC + 16;        // [groups-1][5][128] floats
+  static constexpr int BYTES = OFF_XCH + (kGroups - 1) * 5 * kBlockM * 4;
   static constexpr int ALLOC = BYTES + 1024;  // slack to align the base to 1024
 };
 
@@ -54,35 +57,32 @@ struct RowState {
   float r1, l1, r2, l2, acc;  // r_t in log2 units; acc in raw dot-product units
 };
 
-// Fold one 64-column chunk of a row into the state. a = S1 row values, b = S2
+// Fold one 32-column chunk of a row into the state. a = S1 row values, b = S2
 // (raw dot products). With MASK, keys >= lim are excluded.
 template <bool MASK>
-__device__ __forceinline__ void fold_chunk(float (&a)[64], float (&b)[64], int key0, int lim,
+__device__ __forceinline__ void fold_chunk(float (&a)[32], float (&b)[32], int key0, int lim,
                                            float c, RowState& st) {
   if (MASK) {
 #pragma unroll
-    for (int k = 0; k < 64; ++k) {
+    for (int k = 0; k < 32; ++k) {
       if (key0 + k >= lim) {
         a[k] = -INFINITY;
         b[k] = -INFINITY;
       }
     }
   }
-  float x1[22], x2[22];
+  float x1[11], x2[11];
 #pragma unroll
-  for (int k = 0; k < 21; ++k) {
+  for (int k = 0; k < 10; ++k) {
     x1[k] = max3(a[3 * k], a[3 * k + 1], a[3 * k + 2]);
     x2[k] = max3(b[3 * k], b[3 * k + 1], b[3 * k + 2]);
   }
-  x1[21] = a[63];
-  x2[21] = b[63];
-#pragma unroll
-  for (int k = 0; k < 7; ++k) {
-    x1[k] = max3(x1[3 * k], x1[3 * k + 1], x1[3 * k + 2]);
-    x2[k] = max3(x2[3 * k], x2[3 * k + 1], x2[3 * k + 2]);
-  }
-  float cm1 = max3(max3(x1[0], x1[1], x1[2]), max3(x1[3], x1[4], x1[5]), fmaxf(x1[6], x1[21]));
-  float cm2 = max3(max3(x2[0], x2[1], x2[2]), max3(x2[3], x2[4], x2[5]), fmaxf(x2[6], x2[21]));
+  x1[10] = fmaxf(a[30], a[31]);
+  x2[10] = fmaxf(b[30], b[31]);
+  const float cm1 = max3(max3(x1[0], x1[1], x1[2]), max3(x1[3], x1[4], x1[5]),
+                         max3(max3(x1[6], x1[7], x1[8]), x1[9], x1[10]));
+  const float cm2 = max3(max3(x2[0], x2[1], x2[2]), max3(x2[3], x2[4], x2[5]),
+                         max3(max3(x2[6], x2[7], x2[8]), x2[9], x2[10]));
   if (MASK && cm1 == -INFINITY) return;  // no allowed key in this chunk
   const float t1 = cm1 * c, t2 = cm2 * c;
   if (t1 > st.r1 + kTau) {
@@ -95,21 +95,32 @@ __device__ __forceinline__ void fold_chunk(float (&a)[64], float (&b)[64], int k
     st.l2 *= ex2(st.r2 - t2);
     st.r2 = t2;
   }
-  float l1p[4] = {0.f, 0.f, 0.f, 0.f}, l2p[4] = {0.f, 0.f, 0.f, 0.f}, ap[4] = {0.f, 0.f, 0.f, 0.f};
-  const float nr1 = -st.r1, nr2 = -st.r2;
+  const float2 c2 = make_float2(c, c), m1 = make_float2(-1.f, -1.f);
+  const float2 nr1 = make_float2(-st.r1, -st.r1), nr2 = make_float2(-st.r2, -st.r2);
+  float2 l1p[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float2 l2p[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float2 ap[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-  for (int k = 0; k < 64; ++k) {
-    const float p1 = ex2(fmaf(a[k], c, nr1));
-    const float p2 = ex2(fmaf(b[k], c, nr2));
-    l1p[k & 3] += p1;
-    l2p[k & 3] += p2;
-    float dd = a[k] - b[k];
-    if (MASK) dd = (a[k] == -INFINITY) ? 0.f : dd;
-    ap[k & 3] = fmaf(p1, dd, ap[k & 3]);
+  for (int k = 0; k < 32; k += 2) {
+    const float2 s1 = make_float2(a[k], a[k + 1]), s2 = make_float2(b[k], b[k + 1]);
+    const float2 x1 = __ffma2_rn(s1, c2, nr1), x2 = __ffma2_rn(s2, c2, nr2);
+    const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+    const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+    const int h = (k >> 1) & 1;
+    l1p[h] = __fadd2_rn(l1p[h], p1);
+    l2p[h] = __fadd2_rn(l2p[h], p2);
+    float2 dd = __ffma2_rn(s2, m1, s1);  // s1 - s2
+    if (MASK) {
+      if (a[k] == -INFINITY) dd.x = 0.f;
+      if (a[k + 1] == -INFINITY) dd.y = 0.f;
+    }
+    ap[h] = __ffma2_rn(p1, dd, ap[h]);
   }
-  st.l1 += (l1p[0] + l1p[1]) + (l1p[2] + l1p[3]);
-  st.l2 += (l2p[0] + l2p[1]) + (l2p[2] + l2p[3]);
-  st.acc += (ap[0] + ap[1]) + (ap[2] + ap[3]);
+  const float2 l1s = __fadd2_rn(l1p[0], l1p[1]), l2s = __fadd2_rn(l2p[0], l2p[1]);
+  const float2 as = __fadd2_rn(ap[0], ap[1]);
+  st.l1 += l1s.x + l1s.y;
+  st.l2 += l2s.x + l2s.y;
+  st.acc += as.x + as.y;
 }
 
 // Merge state y into x (same row, disjoint key sets).
@@ -179,7 +190,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     }
     for (int k = 0; k < 2; ++k) {
       mbar_init(s_full(k), 1);
-      mbar_init(s_empty(k), 8);  // one arrival per softmax warp
+      mbar_init(s_empty(k), 4 * kGroups);  // one arrival per softmax warp
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -248,15 +259,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         const uint32_t kbase = sb + L::OFF_K + s * 2 * L::TILE;
         const uint32_t d1 = tmem + slot * 256, d2 = d1 + 128;
+        // the two GEMMs' k-steps interleaved: independent accumulators keep
+        // the tensor pipe busy where one dependent chain would stall it
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
           mma_bf16(d1, smem_desc_sw128(sb + L::OFF_Q1 + koff, 16, 1024),
                    smem_desc_sw128(kbase + koff, 16, 1024), idesc, k > 0);
-        }
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t koff = (k >> 2) * 16384 + (k & 3) * 32;
           mma_bf16(d2, smem_desc_sw128(sb + L::OFF_Q2 + koff, 16, 1024),
                    smem_desc_sw128(kbase + L::TILE + koff, 16, 1024), idesc, k > 0);
         }
@@ -266,51 +275,54 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mma_commit(drain);
       wait_drain(drain, 0, timeout_ns);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 2) {
     // ------------------------------------------------------------ softmax / KL
-    const int wg = (warp - 4) >> 2;
+    const int grp = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const int qrow = qb * kBlockM + r;
     const float c = scale * kLog2e;
     const int lim = causal ? min(NK, qrow + 1 + off) : NK;
     RowState st{-INFINITY, 0.f, -INFINITY, 0.f, 0.f};
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + wg * 64;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * 32;
     for (int it = 0; it < n_iter; ++it) {
       const int slot = it & 1;
       const uint32_t sph = (it >> 1) & 1;
       if (!wait_bounded(s_full(slot), sph, wc)) break;
       tc_fence_after();
-      float a[64], b[64];
+      float a[32], b[32];
       const uint32_t ta = lane_base + slot * 256;
-      tmem_ld32(ta, *reinterpret_cast<float(*)[32]>(&a[0]));
-      tmem_ld32(ta + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
-      tmem_ld32(ta + 128, *reinterpret_cast<float(*)[32]>(&b[0]));
-      tmem_ld32(ta + 160, *reinterpret_cast<float(*)[32]>(&b[32]));
+      tmem_ld32(ta, a);
+      tmem_ld32(ta + 128, b);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_empty(slot));
-      const int key0 = (t_begin + it) * kBlockN + wg * 64;
-      if (key0 + 64 <= lim)
+      const int key0 = (t_begin + it) * kBlockN + grp * 32;
+      if (key0 + 32 <= lim)
         fold_chunk<false>(a, b, key0, lim, c, st);
       else
         fold_chunk<true>(a, b, key0, lim, c, st);
     }
-    // merge the two column halves of each row
+    // merge the column groups' states of each row into group 0
     float* xch = reinterpret_cast<float*>(gb + L::OFF_XCH);
-    if (wg == 1) {
-      xch[0 * kBlockM + r] = st.r1;
-      xch[1 * kBlockM + r] = st.l1;
-      xch[2 * kBlockM + r] = st.r2;
-      xch[3 * kBlockM + r] = st.l2;
-      xch[4 * kBlockM + r] = st.acc;
+    if (grp > 0) {
+      float* x = xch + (grp - 1) * 5 * kBlockM;
+      x[0 * kBlockM + r] = st.r1;
+      x[1 * kBlockM + r] = st.l1;
+      x[2 * kBlockM + r] = st.r2;
+      x[3 * kBlockM + r] = st.l2;
+      x[4 * kBlockM + r] = st.acc;
     }
-    named_bar_sync(1, 256);
-    if (wg == 0) {
-      const RowState other{xch[0 * kBlockM + r], xch[1 * kBlockM + r], xch[2 * kBlockM + r],
-                           xch[3 * kBlockM + r], xch[4 * kBlockM + r]};
-      merge_state(st, other);
+    named_bar_sync(1, 32 * 4 * kGroups);
+    if (grp == 0) {
+#pragma unroll
+      for (int gq = 0; gq < kGroups - 1; ++gq) {
+        const float* x = xch + gq * 5 * kBlockM;
+        const RowState other{x[0 * kBlockM + r], x[1 * kBlockM + r], x[2 * kBlockM + r],
+                             x[3 * kBlockM + r], x[4 * kBlockM + r]};
+        merge_state(st, other);
+      }
       if (qrow < NQ) {
         const size_t o = static_cast<size_t>(bh) * NQ + qrow;
         if (SPLIT) {

@@ -46,14 +46,35 @@ struct BwdArgs {
   uint64_t timeout_ns;
 };
 
+struct BwdSepArgs {
+  const CUtensorMap* tm_q1;  // 64 x 128 boxes, as for the other kernels
+  const CUtensorMap* tm_k1;
+  const CUtensorMap* tm_q2;
+  const CUtensorMap* tm_k2;
+  int BH, NQ, NK, d, causal, grad1;
+  float scale;
+  const float* kl;
+  const float* lse1;
+  const float* lse2;
+  const float* g;
+  void* dq2;  // bf16 outputs
+  void* dk2;
+  void* dq1;  // grad1 only
+  void* dk1;
+  int* dev_status;
+  uint64_t timeout_ns;
+};
+
 // Each returns the launch error (cudaSuccess when queued).
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_combine(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_separate(const BwdSepArgs& a, cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* acc, void* out_bf16, long long n, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* dev_status, uint64_t timeout_ns, cudaStream_t stream);
 
 size_t fwd_smem_bytes(int d);
 size_t bwd_smem_bytes(int d, int grad1);
+size_t bwd_sep_smem_bytes(int d, int grad1);
 
 }  // namespace skl

@@ -70,8 +70,31 @@ size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int caus
                                    int num_splits);
 
 /*
- * Workspace bytes the backward pass needs: one fp32 [B, H, N_Q, d] dQ
- * accumulator per requested gradient set (two when want_grad1 != 0).
+ * Backward algorithm used for these sizes (gist.science technical summary,
+ * section 2, kernel fusion paragraph: a fused kernel with atomic dQ updates,
+ * or separate kernels when the atomics contend too much):
+ *   0 = separate dK and dQ kernels: each keeps its accumulators on chip for
+ *       its whole sweep; no atomics, no workspace (the default);
+ *   1 = one fused kernel per key tile: dK on chip, dQ reduced into an fp32
+ *       workspace with global atomics, then converted to bf16.
+ * Returns -1 on invalid sizes.
+ */
+int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int want_grad1);
+
+/*
+ * Process-wide override of that choice: -1 = automatic, 0 = separate,
+ * 1 = fused. Its initial value comes from the environment variable
+ * STREAMKL_BWD_ALGO=separate|fused (automatic when unset). The workspace
+ * size queries follow it; change it only while no other host thread is
+ * between a size query and the matching streamkl_bwd call. Returns 0, or -1
+ * for an invalid value.
+ */
+int streamkl_set_bwd_algorithm(int algo);
+
+/*
+ * Workspace bytes the backward pass needs: 0 for the separate-kernel
+ * algorithm; for the fused one, one fp32 [B, H, N_Q, d] dQ accumulator per
+ * requested gradient set (two when want_grad1 != 0).
  */
 size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal,
                                    int want_grad1);
@@ -138,8 +161,8 @@ streamkl_status streamkl_fwd_noalloc(const void* q1, const void* k1, const void*
  *        per row (fp32 [B, H, N_Q]).
  *   out: dq2 [B,H,N_Q,d], dk2 [B,H,N_K,d] (bf16); dq1, dk1 likewise, or both
  *        NULL to skip configuration 2 (one NULL and one not is an error).
- *   workspace: ws_bytes >= streamkl_bwd_workspace_size(..., want_grad1); the
- *        call clears the part it uses (stream-ordered).
+ *   workspace: ws_bytes >= streamkl_bwd_workspace_size(..., want_grad1) (may be
+ *        NULL when that is 0); the call clears the part it uses (stream-ordered).
  */
 streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, const void* k2,
                              int B, int H, int NQ, int NK, int d, float scale, int causal,

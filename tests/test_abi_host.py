@@ -58,10 +58,20 @@ def test_split_choice(lib):
 def test_workspace_sizes(lib):
     assert lib.streamkl_fwd_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 5 * 8 * 128 * 512 * 4
     assert lib.streamkl_fwd_workspace_size(4, 32, 512, 131072, 128, 1, 1) == 0
-    assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 1) == 2 * 32 * 65536 * 128 * 4
-    assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 0) == 32 * 65536 * 128 * 4
-    assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == max(
-        5 * 8 * 128 * 512 * 4, 128 * 512 * 128 * 4)
+    try:
+        assert lib.streamkl_set_bwd_algorithm(1) == 0  # fused: fp32 dQ accumulators
+        assert lib.streamkl_bwd_algorithm(1, 32, 65536, 65536, 128, 1, 1) == 1
+        assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 1) == 2 * 32 * 65536 * 128 * 4
+        assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 0) == 32 * 65536 * 128 * 4
+        assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == max(
+            5 * 8 * 128 * 512 * 4, 128 * 512 * 128 * 4)
+        assert lib.streamkl_set_bwd_algorithm(0) == 0  # separate: no workspace
+        assert lib.streamkl_bwd_algorithm(1, 32, 65536, 65536, 128, 1, 1) == 0
+        assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 1) == 0
+        assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 5 * 8 * 128 * 512 * 4
+        assert lib.streamkl_set_bwd_algorithm(7) == -1
+    finally:
+        lib.streamkl_set_bwd_algorithm(-1)
 
 
 def test_forced_split_workspace_rounding(lib):
@@ -100,9 +110,13 @@ def test_backward_validation(lib):
 
     assert bwd(0x1000, 0) == 1  # dq1 without dk1
     assert bwd(0, 0x1000) == 1
-    assert bwd(0, 0, ws=0) == 1  # no workspace
-    assert bwd(0, 0, ws_bytes=16) == 1  # workspace too small
-    assert b"workspace" in lib.streamkl_last_error()
+    try:
+        lib.streamkl_set_bwd_algorithm(1)  # the fused algorithm needs a workspace
+        assert bwd(0, 0, ws=0) == 1
+        assert bwd(0, 0, ws_bytes=16) == 1
+        assert b"workspace" in lib.streamkl_last_error()
+    finally:
+        lib.streamkl_set_bwd_algorithm(-1)
 
 
 def test_selftest_validation(lib):

@@ -43,17 +43,26 @@ def host(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def run(w, seed=0, grad1=None, splits=0, inputs=None):
+def run(w, seed=0, grad1=None, splits=0, inputs=None, algo=None):
+    """Forward + backward through the C ABI. algo: None = the library's choice,
+    binding.BWD_SEPARATE or binding.BWD_FUSED."""
     grad1 = w.grad1 if grad1 is None else grad1
     dev = torch.device("cuda")
     q1, k1, q2, k2, g = inputs if inputs is not None else synthetic.make_inputs(w, seed, dev)
     status = binding.new_status(dev)
     kl, lse1, lse2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, num_splits=splits,
                                           dev_status=status)
-    grads = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
-                                 grad1=grad1, dev_status=status)
+    binding.set_bwd_algorithm(algo)
+    try:
+        grads = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                     grad1=grad1, dev_status=status)
+    finally:
+        binding.set_bwd_algorithm(None)
     binding.raise_on_device_status(status, w.name)
     return (q1, k1, q2, k2, g), (kl, lse1, lse2), grads
+
+
+ALGOS = [pytest.param(0, id="separate"), pytest.param(1, id="fused")]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -70,8 +79,8 @@ def test_bounded_wait_times_out_cleanly():
     assert float(x.sum().item()) == 4.0
 
 
-def full_check(w, seed=0, grad1=True, splits=0):
-    ins, (kl, l1, l2), grads = run(w, seed, grad1, splits)
+def full_check(w, seed=0, grad1=True, splits=0, algo=None):
+    ins, (kl, l1, l2), grads = run(w, seed, grad1, splits, algo=algo)
     h = [host(t) for t in ins[:4]]
     okl, ol1, ol2 = orc.forward(*h, w.scale, w.causal)
     assert_kl(kl.cpu().numpy(), okl)
@@ -85,12 +94,14 @@ def full_check(w, seed=0, grad1=True, splits=0):
         assert grads[2] is None and grads[3] is None
 
 
-def test_tiny_workload_forward_and_backward():
-    full_check(synthetic.WORKLOADS["tiny"], seed=0, grad1=False)
+@pytest.mark.parametrize("algo", ALGOS)
+def test_tiny_workload_forward_and_backward(algo):
+    full_check(synthetic.WORKLOADS["tiny"], seed=0, grad1=False, algo=algo)
 
 
-def test_tiny_workload_both_gradient_sets():
-    full_check(synthetic.WORKLOADS["tiny"], seed=1, grad1=True)
+@pytest.mark.parametrize("algo", ALGOS)
+def test_tiny_workload_both_gradient_sets(algo):
+    full_check(synthetic.WORKLOADS["tiny"], seed=1, grad1=True, algo=algo)
 
 
 RAGGED = [
@@ -99,26 +110,38 @@ RAGGED = [
 ]
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("NQ,NK,d,causal", RAGGED)
-def test_ragged_shapes(NQ, NK, d, causal):
+def test_ragged_shapes(NQ, NK, d, causal, algo):
     w = synthetic.custom(f"ragged{NQ}x{NK}d{d}", B=2, H=3, NQ=NQ, NK=NK, d=d, causal=causal,
                          noise=0.5, grad1=True)
-    full_check(w, seed=NQ + NK)
+    full_check(w, seed=NQ + NK, algo=algo)
 
 
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("NQ,NK,d,causal", [(200, 333, 128, True), (333, 200, 64, False),
+                                            (256, 640, 128, False)])
+def test_ragged_shapes_one_gradient_set(NQ, NK, d, causal, algo):
+    w = synthetic.custom(f"ragged1set{NQ}x{NK}d{d}", B=2, H=3, NQ=NQ, NK=NK, d=d, causal=causal,
+                         noise=0.5)
+    full_check(w, seed=NQ * 3 + NK, grad1=False, algo=algo)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("d", [64, 128])
-def test_peaked_teacher_independent_student(d):
+def test_peaked_teacher_independent_student(d, algo):
     w = synthetic.custom("peaked", B=1, H=2, NQ=384, NK=640, d=d, causal=False, teacher_std=3.0,
                          student="independent", grad1=True)
-    full_check(w, seed=5)
+    full_check(w, seed=5, algo=algo)
 
 
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("causal", [False, True])
-def test_identical_inputs_give_exact_zero(causal):
+def test_identical_inputs_give_exact_zero(causal, algo):
     w = synthetic.custom("same", B=1, H=2, NQ=256, NK=384, d=128, causal=causal, noise=0.0,
                          grad1=True)
     q1, k1, _, _, g = synthetic.make_inputs(w, 3, torch.device("cuda"))
-    _, (kl, l1, l2), grads = run(w, inputs=(q1, k1, q1, k1, g))
+    _, (kl, l1, l2), grads = run(w, inputs=(q1, k1, q1, k1, g), algo=algo)
     assert torch.all(kl == 0)
     assert torch.equal(l1, l2)
     for t in grads:
@@ -138,14 +161,14 @@ def test_split_invariance(splits):
     assert torch.allclose(kl, ref_kl, rtol=1e-4, atol=1e-5)
 
 
-def sampled_check(w, heads, rows, key_sets, seed=0):
+def sampled_check(w, heads, rows, key_sets, seed=0, algo=None):
     """Full-size GPU run; oracle on sampled heads/rows/keys.
 
     rows: query rows whose KL, lse and dQ are compared.
     key_sets: key index arrays whose dK is compared; the oracle sums over every
     query row that can see them.
     """
-    ins, (kl, l1, l2), grads = run(w, seed)
+    ins, (kl, l1, l2), grads = run(w, seed, algo=algo)
     g_all = ins[4]
     n_sets = 4 if w.grad1 else 2
     for (b, hh) in heads:
@@ -197,13 +220,15 @@ def test_stress_workload_full_size():
                   key_sets=[np.arange(w.NK - 128, w.NK)])
 
 
-def test_splitk_workload_full_size():
+@pytest.mark.parametrize("algo", ALGOS)
+def test_splitk_workload_full_size(algo):
     w = synthetic.WORKLOADS["splitk"]
     sampled_check(w, heads=[(0, 0), (3, 31)], rows=np.arange(w.NQ),
-                  key_sets=[np.arange(0, 64), np.arange(w.NK - 600, w.NK)])
+                  key_sets=[np.arange(0, 64), np.arange(w.NK - 600, w.NK)], algo=algo)
 
 
-def test_causal64k_workload_full_size():
+@pytest.mark.parametrize("algo", ALGOS)
+def test_causal64k_workload_full_size(algo):
     w = synthetic.WORKLOADS["causal64k"]
     sampled_check(w, heads=[(0, 0), (0, 31)], rows=_rows(w.NQ, 256, 3),
-                  key_sets=[np.arange(w.NK - 256, w.NK)])
+                  key_sets=[np.arange(w.NK - 256, w.NK)], algo=algo)
