@@ -61,9 +61,11 @@ struct SepLayout {
   static constexpr int OFF_Y = 2 * TILE;  // stage s: Y1 at +2s*TILE, Y2 at +(2s+1)*TILE
   static constexpr int OFF_DS = OFF_Y + 4 * TILE;
   static constexpr int OFF_BAR = OFF_DS + NDS * DS_TILE;
-  // x_full, y_full[2], y_empty[2], s_full, s_free, ds_full[2], ds_free[2],
-  // acc_full, drain
-  static constexpr int NBAR = 13;
+  // x_full, y_full[2], y2_empty[2], s_full, s_free, ds_full[4], ds_free[2],
+  // acc_full, drain, y1_empty[2]. With a shared dS buffer, ds_full is per
+  // (set, half) and ds_free per half; otherwise per set/buffer. Each streamed
+  // tensor's slot is released as soon as its own gradient GEMM is done.
+  static constexpr int NBAR = 17;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;
@@ -130,13 +132,14 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   const uint32_t bar0 = sb + L::OFF_BAR;
   const uint32_t x_full = bar0;
   auto y_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto y_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto y2_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto y1_empty = [&](int s) { return bar0 + 8u * (15 + s); };
   const uint32_t s_full = bar0 + 8u * 5;
   const uint32_t s_free = bar0 + 8u * 6;
   auto ds_full = [&](int t) { return bar0 + 8u * (7 + t); };
-  auto ds_free = [&](int b) { return bar0 + 8u * (9 + b); };
-  const uint32_t acc_full = bar0 + 8u * 11;
-  const uint32_t drain = bar0 + 8u * 12;
+  auto ds_free = [&](int b) { return bar0 + 8u * (11 + b); };
+  const uint32_t acc_full = bar0 + 8u * 13;
+  const uint32_t drain = bar0 + 8u * 14;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
   volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
@@ -145,10 +148,12 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     mbar_init(x_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(y_full(s), 1);
-      mbar_init(y_empty(s), 1);
-      mbar_init(ds_full(s), kSoftmaxWarps);  // one arrival per softmax warp
+      mbar_init(y1_empty(s), 1);
+      mbar_init(y2_empty(s), 1);
       mbar_init(ds_free(s), 1);
     }
+    // one arrival per softmax warp writing the (set, half) or set
+    for (int t = 0; t < 4; ++t) mbar_init(ds_full(t), L::SHARED_DS ? kSoftmaxWarps / 2 : kSoftmaxWarps);
     mbar_init(s_full, 1);
     mbar_init(s_free, kSoftmaxWarps);
     mbar_init(acc_full, 1);
@@ -187,14 +192,24 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       int it = 0;
       for (; it < n_iter; ++it) {
         const int s = it & 1;
-        if (!wait_bounded(y_empty(s), ((it >> 1) & 1) ^ 1, wc)) break;
-        mbar_arrive_expect_tx(y_full(s), 2 * L::TILE);
+        const uint32_t ph = ((it >> 1) & 1) ^ 1;
         const int yrow = (y_begin + it) * kBlockM;
         const uint32_t dst = sb + L::OFF_Y + s * 2 * L::TILE;
+        // Y2's slot frees first (set 2's GEMM runs first): load it as soon as it does
+        if (!wait_bounded(y2_empty(s), ph, wc)) break;
+        mbar_arrive_expect_tx(y_full(s), 2 * L::TILE);
 #pragma unroll
-        for (int b = 0; b < L::KB; ++b) {
-          tma_load_3d(dst + b * 16384, &tm_y1, y_full(s), b * 64, yrow, bh);
+        for (int b = 0; b < L::KB; ++b)
           tma_load_3d(dst + L::TILE + b * 16384, &tm_y2, y_full(s), b * 64, yrow, bh);
+        const bool y1_ok = wait_bounded(y1_empty(s), ph, wc);
+        if (y1_ok) {
+#pragma unroll
+          for (int b = 0; b < L::KB; ++b)
+            tma_load_3d(dst + b * 16384, &tm_y1, y_full(s), b * 64, yrow, bh);
+        }
+        if (!y1_ok) {
+          ++it;  // Y2 of this tile is in flight: count it for the drain below
+          break;
         }
       }
       // let every copy this thread issued land before the CTA can exit
@@ -239,24 +254,30 @@ __global__ void __launch_bounds__(kSepThreads, 1)
           const uint32_t y1 = sb + L::OFF_Y + (j & 1) * 2 * L::TILE, y2 = y1 + L::TILE;
           const uint32_t acc2 = tmem + L::COL_ACC, acc1 = acc2 + D;
           const uint32_t ds0 = sb + L::OFF_DS;
-          if (!(ok = wait_bounded(ds_full(0), j & 1, wc))) break;
-          if (!L::SHARED_DS && GRAD1 && !(ok = wait_bounded(ds_full(1), j & 1, wc))) break;
-          tc_fence_after();
           if (L::SHARED_DS) {
-            // the two sets take turns in one dS buffer: set 2, then set 1
+            // The two sets take turns in one dS buffer (set 2, then set 1), half
+            // by half: k-steps 0-3 read half 0 (keys 0-63 in the dQ kernel,
+            // query rows 0-63 in the dK kernel), 4-7 half 1, and each half is
+            // handed back as soon as its k-steps are done.
+            for (int t = 0; ok && t < 2; ++t) {
+              const uint32_t acc = t == 0 ? acc2 : acc1;
+              const uint32_t yt = t == 0 ? y2 : y1;
+              for (int h = 0; h < 2; ++h) {
+                if (!(ok = wait_bounded(ds_full(t * 2 + h), j & 1, wc))) break;
+                tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_bf16(acc2, a_desc(ds0, k), smem_desc_sw128(y2 + k * 2048, 16384, 1024), id_g,
-                       (j > 0 || k > 0));
-            mma_commit(ds_free(0));
-            if (!(ok = wait_bounded(ds_full(1), j & 1, wc))) break;
-            tc_fence_after();
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              mma_bf16(acc1, a_desc(ds0, k), smem_desc_sw128(y1 + k * 2048, 16384, 1024), id_g,
-                       (j > 0 || k > 0));
-            mma_commit(ds_free(0));
+                for (int k = 4 * h; k < 4 * h + 4; ++k)
+                  mma_bf16(acc, a_desc(ds0, k), smem_desc_sw128(yt + k * 2048, 16384, 1024), id_g,
+                           (j > 0 || k > 0));
+                mma_commit(ds_free(h));
+              }
+              mma_commit(t == 0 ? y2_empty(j & 1) : y1_empty(j & 1));
+            }
+            if (!ok) break;
           } else {
+            if (!(ok = wait_bounded(ds_full(0), j & 1, wc))) break;
+            if (GRAD1 && !(ok = wait_bounded(ds_full(1), j & 1, wc))) break;
+            tc_fence_after();
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
               mma_bf16(acc2, a_desc(ds0, k), smem_desc_sw128(y2 + k * 2048, 16384, 1024), id_g,
@@ -267,8 +288,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
             }
             mma_commit(ds_free(0));
             if (GRAD1) mma_commit(ds_free(1));
+            mma_commit(y2_empty(j & 1));
+            mma_commit(y1_empty(j & 1));
           }
-          mma_commit(y_empty(j & 1));
         }
       }
       mma_commit(acc_full);
@@ -291,6 +313,18 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       return load_row_const(lse1_in, lse2_in, g_in, kl_in, rowbase + q, scale,
                             it < n_iter && q < NQ);
     };
+    // dK kernel: raw per-row values of the next tile, loaded a whole tile ahead
+    // and only turned into constants when that tile starts
+    auto load_raw = [&](int it, float4& v) {
+      const int q = qrow_of(it);
+      v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (it < n_iter && q < NQ) {
+        const size_t o = rowbase + q;
+        v = make_float4(lse1_in[o], lse2_in[o], g_in[o], kl_in[o]);
+      }
+    };
+    // half of the shared dS buffer this thread's values land in
+    const int half = DQ ? (grp >> 1) : (quarter >> 1);
     // write this thread's 32 bf16 dS values (keys [32 grp, +32) of row r)
     // into buffer `buf`: half grp/2 of the tile, 16-byte chunks 4 (grp%2) + j
     auto write_ds = [&](int buf, const float (&v)[32]) {
@@ -306,7 +340,8 @@ __global__ void __launch_bounds__(kSepThreads, 1)
 
     RowConst rc = load_const(0);
     for (int it = 0; it < n_iter; ++it) {
-      const RowConst nrc = DQ ? rc : load_const(it + 1);  // prefetch the next tile's row
+      float4 nraw;
+      if (!DQ) load_raw(it + 1, nraw);
       const int qrow = qrow_of(it);
       const int key0 = (DQ ? (y_begin + it) * kBlockN : x0) + grp * 32;
       const int lim = causal ? min(NK, qrow + 1 + off) : NK;  // keys < lim visible
@@ -347,16 +382,16 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       }
       const uint32_t par = it & 1;
       if (L::SHARED_DS) {
-        // set 2 waits for the set-1 GEMM of the previous tile, set 1 for the
-        // set-2 GEMM of this tile (the buffer's completions alternate)
-        if (!(ok = wait_bounded(ds_free(0), 1, wc))) break;
+        // per half: set 2 waits for the set-1 GEMM of the previous tile, set 1
+        // for the set-2 GEMM of this tile (the half's completions alternate)
+        if (!(ok = wait_bounded(ds_free(half), 1, wc))) break;
         write_ds(0, b);
         __syncwarp();
-        if (lane == 0) mbar_arrive(ds_full(0));
-        if (!(ok = wait_bounded(ds_free(0), 0, wc))) break;
+        if (lane == 0) mbar_arrive(ds_full(half));
+        if (!(ok = wait_bounded(ds_free(half), 0, wc))) break;
         write_ds(0, a);
         __syncwarp();
-        if (lane == 0) mbar_arrive(ds_full(1));
+        if (lane == 0) mbar_arrive(ds_full(2 + half));
       } else {
         if (!(ok = wait_bounded(ds_free(0), par ^ 1, wc))) break;
         write_ds(0, b);
@@ -370,7 +405,12 @@ __global__ void __launch_bounds__(kSepThreads, 1)
           if (GRAD1) mbar_arrive(ds_full(1));
         }
       }
-      rc = nrc;
+      if (!DQ) {
+        rc.b1 = nraw.x * kLog2e;
+        rc.b2 = nraw.y * kLog2e;
+        rc.gs = nraw.z * scale;
+        rc.e = nraw.x - nraw.y + nraw.w;
+      }
     }
     // epilogue: accumulator row r -> bf16 dQ (dQ kernel) or dK (dK kernel) row
     if (ok && n_iter > 0 && wait_bounded(acc_full, 0, wc)) {

@@ -327,26 +327,39 @@ def gpu_arm(args, w):
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
 
     f_fwd, f_bwd_metric, f_bwd_work, f_fwd_exact, f_bwd_exact = flop_counts(w)
+    algo = binding.bwd_algorithm(B, H, NQ, NK, d, w.causal, w.grad1)
+    pairs = w.live_pairs_per_head() * B * H
+    if algo == binding.BWD_SEPARATE:
+        # the dK and dQ kernels each recompute S1 and S2 (4d FLOPs per pair) and
+        # add one d x 2 GEMM per gradient set
+        f_bwd_exact = (8 + (8 if w.grad1 else 4)) * pairs * d
+        bwd_name = "streamkl_bwd_sep_kernel (dK + dQ)"
+        bwd_note = "separate dK and dQ kernels, timed together (one API call)"
+    else:
+        bwd_name = "streamkl_bwd_kernel"
+        bwd_note = "fused kernel; includes the workspace clear and the fp32->bf16 dQ conversion"
     step_flops = f_fwd + f_bwd_metric
     value = world * step_flops / (ms_step * 1e-3) / 1e12
     pk = peaks()
     sustained = pk["bf16_tflops_sustained"]
-    # per-kernel rooflines; the backward launch (kernel + dQ convert) is the larger
     fwd_tf = f_fwd_exact / (fwd_ms * 1e-3) / 1e12
     bwd_tf = f_bwd_exact / (bwd_ms * 1e-3) / 1e12
     kernels = {
         "streamkl_fwd_kernel": {"ms": fwd_ms, "algorithmic_tflop": f_fwd_exact / 1e12,
                                 "achieved_tflops": fwd_tf, "frac_of_measured_sustained": fwd_tf / sustained},
-        "streamkl_bwd_kernel": {"ms": bwd_ms, "algorithmic_tflop": f_bwd_exact / 1e12,
-                                "achieved_tflops": bwd_tf, "frac_of_measured_sustained": bwd_tf / sustained,
-                                "note": "includes the fp32->bf16 dQ conversion and workspace clear"},
+        bwd_name: {"ms": bwd_ms, "algorithmic_tflop": f_bwd_exact / 1e12,
+                   "achieved_tflops": bwd_tf, "frac_of_measured_sustained": bwd_tf / sustained,
+                   "note": bwd_note},
     }
-    dom = "streamkl_bwd_kernel" if bwd_ms >= fwd_ms else "streamkl_fwd_kernel"
+    dom = bwd_name if bwd_ms >= fwd_ms else "streamkl_fwd_kernel"
     dom_tf = kernels[dom]["achieved_tflops"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": sustained,
                 "unit": "TFLOP/s", "frac": dom_tf / sustained, "traffic": None,
                 "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a long step)"}
-    launches_per_step = 1 + (1 if splits > 1 else 0) + 1 + (2 if w.grad1 else 1)
+    if algo == binding.BWD_SEPARATE:
+        launches_per_step = 1 + (1 if splits > 1 else 0) + 2
+    else:
+        launches_per_step = 1 + (1 if splits > 1 else 0) + 1 + (2 if w.grad1 else 1)
 
     e2e = None
     if not args.no_e2e:
@@ -371,6 +384,7 @@ def gpu_arm(args, w):
             "data": "synthetic",
             "config": {"workload": describe(w), "B": B, "H": H, "N_Q": NQ, "N_K": NK, "d": d,
                        "causal": w.causal, "grad1": w.grad1, "splits": splits,
+                       "bwd_algorithm": "separate" if algo == binding.BWD_SEPARATE else "fused",
                        "flop_convention": "4 NQ NK d fwd + 8 NQ NK d bwd per head, halved for causal",
                        "l2": "inputs (2 GiB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
