@@ -166,14 +166,16 @@ size_t bwd_ws(int B, int H, int NQ, int NK, int d, int grad1) {
   return grad1 ? 2 * one : one;
 }
 
-streamkl_status make_map(CUtensorMap* m, const void* ptr, int BH, int N, int d, const char* name) {
+// 3-D map {d, N, B*H} of one bf16 tensor, 64-column x box_rows boxes, 128-byte swizzle.
+streamkl_status make_map(CUtensorMap* m, const void* ptr, int BH, int N, int d, const char* name,
+                         int box_rows = skl::kBlockM) {
   auto enc = encode_fn();
   if (!enc) return fail(STREAMKL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
   const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(d) * 2,
                                  static_cast<cuuint64_t>(N) * d * 2};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(skl::kBlockM), 1};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim, gstride, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -393,11 +395,13 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
     return fail(STREAMKL_ERR_INVALID_ARG, "backward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
 
   const int BH = B * H;
+  // the separate kernels move 64-row boxes, the fused one 128-row boxes
+  const int box_rows = algo == 0 ? 64 : skl::kBlockM;
   CUtensorMap mq1, mk1, mq2, mk2;
-  if ((st = make_map(&mq1, q1, BH, NQ, d, "q1")) != STREAMKL_OK) return st;
-  if ((st = make_map(&mk1, k1, BH, NK, d, "k1")) != STREAMKL_OK) return st;
-  if ((st = make_map(&mq2, q2, BH, NQ, d, "q2")) != STREAMKL_OK) return st;
-  if ((st = make_map(&mk2, k2, BH, NK, d, "k2")) != STREAMKL_OK) return st;
+  if ((st = make_map(&mq1, q1, BH, NQ, d, "q1", box_rows)) != STREAMKL_OK) return st;
+  if ((st = make_map(&mk1, k1, BH, NK, d, "k1", box_rows)) != STREAMKL_OK) return st;
+  if ((st = make_map(&mq2, q2, BH, NQ, d, "q2", box_rows)) != STREAMKL_OK) return st;
+  if ((st = make_map(&mk2, k2, BH, NK, d, "k2", box_rows)) != STREAMKL_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (algo == 0) {

@@ -47,7 +47,7 @@ struct BwdArgs {
 };
 
 struct BwdSepArgs {
-  const CUtensorMap* tm_q1;  // 64 x 128 boxes, as for the other kernels
+  const CUtensorMap* tm_q1;  // 64-column x 64-row boxes
   const CUtensorMap* tm_k1;
   const CUtensorMap* tm_q2;
   const CUtensorMap* tm_k2;
