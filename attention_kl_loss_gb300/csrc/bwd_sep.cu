@@ -300,11 +300,14 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         }
       } else {
         // gradient GEMMs of step j once its dS is in TMEM, queued behind the T
-        // GEMMs of step j+2: the next T is on the softmax warps' critical path,
-        // these GEMMs are not (their dS buffer is next written two steps on)
+        // GEMMs of step j+kGradLag: the next T is on the softmax warps'
+        // critical path, these GEMMs are not (their dS buffer is next written
+        // two steps on). The dQ kernel, bound by the tensor pipe, lags by 2;
+        // the dK kernel, whose shallower Y ring must be released sooner, by 1.
+        constexpr int kGradLag = DQ ? 2 : 1;
         for (int j = 0; j < n_iter; ++j) {
           if (!wait_bounded(ds_full(j & 1), (j >> 1) & 1, wc)) break;
-          const int need = min(j + 3, n_iter);
+          const int need = min(j + kGradLag + 1, n_iter);
           const uint64_t t0 = global_timer_ns();
           while (*t_queued < need && !*abort_flag && global_timer_ns() - t0 < timeout_ns) {
           }
@@ -365,6 +368,7 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         const float* tq = tab + (it % kStages) * 4 * kStepRows + grp * 16;
         const float2 c2 = make_float2(c, c), sc2 = make_float2(scale, scale);
         const float2 m1 = make_float2(-1.f, -1.f);
+        float4 q1c, q2c, qgc, qec;  // dK kernel: 4 columns of each constant, one 16-byte load each
 #pragma unroll
         for (int k = 0; k < 16; k += 2) {
           float2 nb1, nb2, gs, ne;
@@ -374,10 +378,17 @@ __global__ void __launch_bounds__(kSepThreads, 1)
             gs = make_float2(rc.z, rc.z);
             ne = make_float2(-rc.w, -rc.w);
           } else {
-            nb1 = *reinterpret_cast<const float2*>(tq + k);
-            nb2 = *reinterpret_cast<const float2*>(tq + kStepRows + k);
-            gs = *reinterpret_cast<const float2*>(tq + 2 * kStepRows + k);
-            if (GRAD1) ne = *reinterpret_cast<const float2*>(tq + 3 * kStepRows + k);
+            if ((k & 3) == 0) {
+              q1c = *reinterpret_cast<const float4*>(tq + k);
+              q2c = *reinterpret_cast<const float4*>(tq + kStepRows + k);
+              qgc = *reinterpret_cast<const float4*>(tq + 2 * kStepRows + k);
+              if (GRAD1) qec = *reinterpret_cast<const float4*>(tq + 3 * kStepRows + k);
+            }
+            const bool lo = (k & 3) == 0;
+            nb1 = lo ? make_float2(q1c.x, q1c.y) : make_float2(q1c.z, q1c.w);
+            nb2 = lo ? make_float2(q2c.x, q2c.y) : make_float2(q2c.z, q2c.w);
+            gs = lo ? make_float2(qgc.x, qgc.y) : make_float2(qgc.z, qgc.w);
+            if (GRAD1) ne = lo ? make_float2(qec.x, qec.y) : make_float2(qec.z, qec.w);
           }
           const float2 s1 = make_float2(a[k], a[k + 1]), s2 = make_float2(b[k], b[k + 1]);
           const float2 x1 = __ffma2_rn(s1, c2, nb1), x2 = __ffma2_rn(s2, c2, nb2);
