@@ -335,25 +335,33 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       rc = query_const(lse1_in, lse2_in, g_in, kl_in, static_cast<size_t>(bh) * NQ + xrow, scale,
                        xrow < NQ);
 
+    // T of step `it` into a, b (all lanes agree on every wait's outcome, so
+    // the warp-wide TMEM loads and the __syncwarp below are never reached by
+    // part of a warp); then the T GEMMs of step it+1 may overwrite T
+    float a[16], b[16];
+    auto load_t = [&](int it) {
+      if (!__all_sync(0xffffffffu, wait_bounded(s_full, it & 1, wc))) return false;
+      tc_fence_after();
+      tmem_ld16(tmem + lane_off + L::COL_T + grp * 16, a);
+      tmem_ld16(tmem + lane_off + L::COL_T + 64 + grp * 16, b);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free);
+      // dK kernel: the stage's barrier also publishes its constant table
+      return DQ || __all_sync(0xffffffffu, wait_bounded(y_full(it % kStages), (it / kStages) & 1, wc));
+    };
+    // The next step's T is loaded right after this step's dS is computed and
+    // before it is stored, so the next T GEMMs can start as early as possible.
+    bool good = n_iter > 0 && load_t(0);
     for (int it = 0; it < n_iter; ++it) {
-      const int y0 = (y_begin + it) * kStepRows + grp * 16;  // first Y row of this thread's columns
-      // all lanes agree on every wait's outcome, so the warp-wide TMEM loads
-      // and the __syncwarp below are never reached by part of a warp
-      bool good = __all_sync(0xffffffffu, wait_bounded(s_full, it & 1, wc));
-      float a[16], b[16];
-      if (good) {
-        tc_fence_after();
-        tmem_ld16(tmem + lane_off + L::COL_T + grp * 16, a);
-        tmem_ld16(tmem + lane_off + L::COL_T + 64 + grp * 16, b);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_free);  // the T GEMMs of step it+1 may overwrite
-        // dK kernel: the stage's barrier also publishes its constant table
-        if (!DQ) good = __all_sync(0xffffffffu, wait_bounded(y_full(it % kStages), (it / kStages) & 1, wc));
+      if (!good) {
+        ok = false;
+        break;
       }
+      const int y0 = (y_begin + it) * kStepRows + grp * 16;  // first Y row of this thread's columns
       uint32_t d2p[8], d1p[8];
-      if (good) {
+      {
         // visibility of (query, key) over this thread's 16 columns
         bool full;
         int lim = 0;
@@ -407,10 +415,10 @@ __global__ void __launch_bounds__(kSepThreads, 1)
             d1p[k >> 1] = pack_bf16x2(d1.x, d1.y);
           }
         }
-        // the gradient GEMMs of step it-2 have read this dS buffer
-        good = __all_sync(0xffffffffu, wait_bounded(ds_free(it & 1), ((it >> 1) & 1) ^ 1, wc));
       }
-      if (!good) {
+      if (it + 1 < n_iter) good = load_t(it + 1);
+      // the gradient GEMMs of step it-2 have read this dS buffer
+      if (!__all_sync(0xffffffffu, wait_bounded(ds_free(it & 1), ((it >> 1) & 1) ^ 1, wc))) {
         ok = false;
         break;
       }
