@@ -196,9 +196,12 @@ def streamkl_fwd_noalloc(q1, k1, q2, k2, out, scale: Optional[float] = None,
 
 def streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = None,
                  causal: bool = False, grad1: bool = False, out=None, workspace=None,
-                 dev_status=None, stream=None):
-    """Gradients of sum(dkl * KL): (dq2, dk2, dq1, dk1), bf16; dq1/dk1 None
-    unless ``grad1``."""
+                 dev_status=None, stream=None, grad2: bool = True):
+    """Gradients of sum(dkl * KL): (dq2, dk2, dq1, dk1), bf16. dq2/dk2
+    (configuration 1, P1 fixed) unless ``grad2`` is False; dq1/dk1
+    (configuration 2, P2 fixed) only with ``grad1``; skipped ones are None."""
+    if not (grad1 or grad2):
+        raise ValueError("no gradient requested (grad1 and grad2 both False)")
     lib = load()
     B, H, NQ, NK, d = _dims(q1, k1, q2, k2)
     for name, t in (("kl", kl), ("lse1", lse1), ("lse2", lse2), ("dkl", dkl)):
@@ -207,8 +210,8 @@ def streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = N
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dev = q1.device
     if out is None:
-        dq2 = torch.empty_like(q2)
-        dk2 = torch.empty_like(k2)
+        dq2 = torch.empty_like(q2) if grad2 else None
+        dk2 = torch.empty_like(k2) if grad2 else None
         dq1 = torch.empty_like(q1) if grad1 else None
         dk1 = torch.empty_like(k1) if grad1 else None
     else:

@@ -381,16 +381,20 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   if (st != STREAMKL_OK) return st;
   if ((st = check_inputs(q1, k1, q2, k2)) != STREAMKL_OK) return st;
   if (!kl || !lse1 || !lse2 || !dkl) return fail(STREAMKL_ERR_INVALID_ARG, "kl/lse1/lse2/dkl must be non-NULL");
-  if (!dq2 || !dk2) return fail(STREAMKL_ERR_INVALID_ARG, "dq2 and dk2 must be non-NULL");
+  if ((dq2 == nullptr) != (dk2 == nullptr))
+    return fail(STREAMKL_ERR_INVALID_ARG, "dq2 and dk2 must be both NULL or both non-NULL");
   if ((dq1 == nullptr) != (dk1 == nullptr))
     return fail(STREAMKL_ERR_INVALID_ARG, "dq1 and dk1 must be both NULL or both non-NULL");
-  if (!aligned16(dq2) || !aligned16(dk2) || (dq1 && (!aligned16(dq1) || !aligned16(dk1))))
+  if (!dq2 && !dq1) return fail(STREAMKL_ERR_INVALID_ARG, "no gradient requested: dq2/dk2 and dq1/dk1 are all NULL");
+  if ((dq2 && (!aligned16(dq2) || !aligned16(dk2))) || (dq1 && (!aligned16(dq1) || !aligned16(dk1))))
     return fail(STREAMKL_ERR_INVALID_ARG, "gradient outputs must be 16-byte aligned");
   if (!dev_status) return fail(STREAMKL_ERR_INVALID_ARG, "dev_status must be non-NULL");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(STREAMKL_ERR_INVALID_ARG, "scale must be finite and > 0");
-  const int grad1 = dq1 != nullptr;
-  const int algo = bwd_algo_impl(B, H, NQ, NK);
-  const size_t need = bwd_ws(B, H, NQ, NK, d, grad1);
+  const int grad1 = dq1 != nullptr, grad2 = dq2 != nullptr;
+  // configuration 2 alone always runs the separate kernels (the fused kernel
+  // always produces dQ2/dK2)
+  const int algo = grad2 ? bwd_algo_impl(B, H, NQ, NK) : 0;
+  const size_t need = algo == 0 ? 0 : bwd_ws(B, H, NQ, NK, d, grad1);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
     return fail(STREAMKL_ERR_INVALID_ARG, "backward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
 
@@ -416,6 +420,7 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
     a.d = d;
     a.causal = causal;
     a.grad1 = grad1;
+    a.grad2 = grad2;
     a.scale = scale;
     a.kl = kl;
     a.lse1 = lse1;

@@ -57,12 +57,16 @@ constexpr int kSoftmaxWarps = 16;
 constexpr int kStepRows = 64;     // Y rows per step
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <int D, bool DQ, bool GRAD1>
+// Gradient sets a launch computes (bit mask): configuration 1 (P1 fixed)
+// gives dQ2/dK2 from dS2, configuration 2 (P2 fixed) gives dQ1/dK1 from dS1.
+constexpr int kSet2 = 1, kSet1 = 2;
+
+template <int D, bool DQ, int SETS>
 struct SepLayout {
   static constexpr int KB = D / 64;                   // 128-byte boxes per row
   static constexpr int XT = kBlockM * D * 2;          // 128 rows of one X tensor
   static constexpr int YT = kStepRows * D * 2;        // 64 rows of one Y tensor
-  static constexpr int NSETS = GRAD1 ? 2 : 1;
+  static constexpr int NSETS = SETS == (kSet1 | kSet2) ? 2 : 1;
   // as many Y stages as fit next to X (and the dK kernel's tables)
   static constexpr int STAGES = D == 64 ? 8 : (DQ ? 5 : 4);
   static constexpr int OFF_X = 0;                     // X1, X2
@@ -93,7 +97,7 @@ __device__ __forceinline__ float4 query_const(const float* lse1, const float* ls
   return q;
 }
 
-template <int D, bool DQ, bool GRAD1>
+template <int D, bool DQ, int SETS>
 __global__ void __launch_bounds__(kSepThreads, 1)
     streamkl_bwd_sep_kernel(const __grid_constant__ CUtensorMap tm_x1,
                             const __grid_constant__ CUtensorMap tm_x2,
@@ -104,7 +108,8 @@ __global__ void __launch_bounds__(kSepThreads, 1)
                             const float* __restrict__ g_in, __nv_bfloat16* __restrict__ out2,
                             __nv_bfloat16* __restrict__ out1, int* dev_status,
                             uint64_t timeout_ns) {
-  using L = SepLayout<D, DQ, GRAD1>;
+  using L = SepLayout<D, DQ, SETS>;
+  constexpr bool HAS2 = SETS & kSet2, HAS1 = SETS & kSet1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
@@ -266,19 +271,20 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         }
         mma_commit(s_full);
       };
-      // gradient GEMMs of step j: A = dS from TMEM buffer j&1, B = Y MN-major,
-      // the two sets' k-steps interleaved
+      // gradient GEMMs of step j: A = dS from TMEM buffer j&1 (slot t of a
+      // buffer holds the t-th computed set), B = the set's Y (set 2: Y2, set
+      // 1: Y1) MN-major; with two sets their k-steps interleave
       auto issue_g = [&](int j) {
         const uint64_t dy = smem_desc_sw128(sb + L::OFF_Y + (j % kStages) * 2 * L::YT, 8192, 1024);
         const uint32_t dsb = tmem + L::COL_DS + (j & 1) * 64;
 #pragma unroll
-        for (int kg = 0; kg < 4; ++kg) {
-          mma_bf16_ts(tmem + L::COL_ACC, dsb + 8 * kg, desc_advance(dy, L::YT + kg * 2048), id_g,
-                      (j > 0 || kg > 0));
-          if (GRAD1)
-            mma_bf16_ts(tmem + L::COL_ACC + D, dsb + 32 + 8 * kg, desc_advance(dy, kg * 2048), id_g,
-                        (j > 0 || kg > 0));
-        }
+        for (int kg = 0; kg < 4; ++kg)
+#pragma unroll
+          for (int t = 0; t < L::NSETS; ++t) {
+            const bool set2 = HAS2 && t == 0;
+            mma_bf16_ts(tmem + L::COL_ACC + t * D, dsb + 32 * t + 8 * kg,
+                        desc_advance(dy, (set2 ? L::YT : 0) + kg * 2048), id_g, (j > 0 || kg > 0));
+          }
         mma_commit(ds_free(j & 1));
         mma_commit(y_empty(j % kStages));
       };
@@ -390,25 +396,30 @@ __global__ void __launch_bounds__(kSepThreads, 1)
               q1c = *reinterpret_cast<const float4*>(tq + k);
               q2c = *reinterpret_cast<const float4*>(tq + kStepRows + k);
               qgc = *reinterpret_cast<const float4*>(tq + 2 * kStepRows + k);
-              if (GRAD1) qec = *reinterpret_cast<const float4*>(tq + 3 * kStepRows + k);
+              if (HAS1) qec = *reinterpret_cast<const float4*>(tq + 3 * kStepRows + k);
             }
             const bool lo = (k & 3) == 0;
             nb1 = lo ? make_float2(q1c.x, q1c.y) : make_float2(q1c.z, q1c.w);
             nb2 = lo ? make_float2(q2c.x, q2c.y) : make_float2(q2c.z, q2c.w);
             gs = lo ? make_float2(qgc.x, qgc.y) : make_float2(qgc.z, qgc.w);
-            if (GRAD1) ne = lo ? make_float2(qec.x, qec.y) : make_float2(qec.z, qec.w);
+            if (HAS1) ne = lo ? make_float2(qec.x, qec.y) : make_float2(qec.z, qec.w);
           }
           const float2 s1 = make_float2(a[k], a[k + 1]), s2 = make_float2(b[k], b[k + 1]);
-          const float2 x1 = __ffma2_rn(s1, c2, nb1), x2 = __ffma2_rn(s2, c2, nb2);
-          float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
-          float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+          const float2 x1 = __ffma2_rn(s1, c2, nb1);
+          float2 p1 = make_float2(ex2(x1.x), ex2(x1.y)), p2 = p1;
+          if constexpr (HAS2) {  // P2 only for configuration 1
+            const float2 x2 = __ffma2_rn(s2, c2, nb2);
+            p2 = make_float2(ex2(x2.x), ex2(x2.y));
+          }
           if (!full) {
             if (!visible(y0 + k)) p1.x = p2.x = 0.f;
             if (!visible(y0 + k + 1)) p1.y = p2.y = 0.f;
           }
-          const float2 d2 = __fmul2_rn(__ffma2_rn(p1, m1, p2), gs);  // g (P2 - P1)
-          d2p[k >> 1] = pack_bf16x2(d2.x, d2.y);
-          if (GRAD1) {
+          if constexpr (HAS2) {
+            const float2 d2 = __fmul2_rn(__ffma2_rn(p1, m1, p2), gs);  // g (P2 - P1)
+            d2p[k >> 1] = pack_bf16x2(d2.x, d2.y);
+          }
+          if constexpr (HAS1) {
             // g P1 (log(P1/P2) - KL), log(P1/P2) - KL = scale (s1 - s2) - e
             const float2 lr = __ffma2_rn(__ffma2_rn(s2, m1, s1), sc2, ne);
             const float2 d1 = __fmul2_rn(__fmul2_rn(p1, gs), lr);
@@ -423,10 +434,10 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         break;
       }
       // this thread's 16 values of row r: 8 packed columns per set at
-      // [8 grp, 8 grp + 8) of the set's 32-column half of buffer it&1
+      // [8 grp, 8 grp + 8) of the set's 32-column slot of buffer it&1
       const uint32_t dsb = tmem + lane_off + L::COL_DS + (it & 1) * 64 + grp * 8;
-      tmem_st8(dsb, d2p);
-      if (GRAD1) tmem_st8(dsb + 32, d1p);
+      if (HAS2) tmem_st8(dsb, d2p);
+      if (HAS1) tmem_st8(dsb + (HAS2 ? 32 : 0), d1p);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -439,7 +450,7 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       constexpr int EC = D / 4;
 #pragma unroll
       for (int t = 0; t < L::NSETS; ++t) {
-        __nv_bfloat16* out = t == 0 ? out2 : out1;
+        __nv_bfloat16* out = (HAS2 && t == 0) ? out2 : out1;
         float v[EC];
         if constexpr (EC == 32)
           tmem_ld32(tmem + lane_off + L::COL_ACC + t * D + grp * EC, v);
@@ -468,10 +479,10 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   }
 }
 
-template <int D, bool DQ, bool GRAD1>
+template <int D, bool DQ, int SETS>
 cudaError_t launch_sep_t(const BwdSepArgs& a, cudaStream_t stream) {
-  using L = SepLayout<D, DQ, GRAD1>;
-  auto kern = streamkl_bwd_sep_kernel<D, DQ, GRAD1>;
+  using L = SepLayout<D, DQ, SETS>;
+  auto kern = streamkl_bwd_sep_kernel<D, DQ, SETS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int NX = DQ ? a.NQ : a.NK;
@@ -489,14 +500,16 @@ cudaError_t launch_sep_t(const BwdSepArgs& a, cudaStream_t stream) {
 
 template <int D, bool DQ>
 cudaError_t launch_sep_g(const BwdSepArgs& a, cudaStream_t stream) {
-  return a.grad1 ? launch_sep_t<D, DQ, true>(a, stream) : launch_sep_t<D, DQ, false>(a, stream);
+  if (a.grad1 && a.grad2) return launch_sep_t<D, DQ, kSet1 | kSet2>(a, stream);
+  return a.grad1 ? launch_sep_t<D, DQ, kSet1>(a, stream) : launch_sep_t<D, DQ, kSet2>(a, stream);
 }
 
 }  // namespace
 
 size_t bwd_sep_smem_bytes(int d, int grad1) {
-  if (d == 128) return grad1 ? SepLayout<128, false, true>::ALLOC : SepLayout<128, false, false>::ALLOC;
-  return grad1 ? SepLayout<64, false, true>::ALLOC : SepLayout<64, false, false>::ALLOC;
+  constexpr int both = kSet1 | kSet2;
+  if (d == 128) return grad1 ? SepLayout<128, false, both>::ALLOC : SepLayout<128, false, kSet2>::ALLOC;
+  return grad1 ? SepLayout<64, false, both>::ALLOC : SepLayout<64, false, kSet2>::ALLOC;
 }
 
 cudaError_t launch_bwd_separate(const BwdSepArgs& a, cudaStream_t stream) {

@@ -51,13 +51,14 @@ struct BwdSepArgs {
   const CUtensorMap* tm_k1;
   const CUtensorMap* tm_q2;
   const CUtensorMap* tm_k2;
-  int BH, NQ, NK, d, causal, grad1;
+  int BH, NQ, NK, d, causal;
+  int grad1, grad2;  // gradient sets wanted: dQ1/dK1 (configuration 2), dQ2/dK2 (configuration 1)
   float scale;
   const float* kl;
   const float* lse1;
   const float* lse2;
   const float* g;
-  void* dq2;  // bf16 outputs
+  void* dq2;  // bf16 outputs (NULL when grad2 == 0)
   void* dk2;
   void* dq1;  // grad1 only
   void* dk1;

@@ -159,8 +159,11 @@ streamkl_status streamkl_fwd_noalloc(const void* q1, const void* k1, const void*
  *   in : q1, k1, q2, k2, sizes, scale, causal exactly as given to streamkl_fwd;
  *        kl, lse1, lse2 as produced by streamkl_fwd; dkl = upstream gradient
  *        per row (fp32 [B, H, N_Q]).
- *   out: dq2 [B,H,N_Q,d], dk2 [B,H,N_K,d] (bf16); dq1, dk1 likewise, or both
- *        NULL to skip configuration 2 (one NULL and one not is an error).
+ *   out: dq2 [B,H,N_Q,d], dk2 [B,H,N_K,d] (bf16) for configuration 1;
+ *        dq1, dk1 likewise for configuration 2. Either pair may be NULL to
+ *        skip that configuration (both of a pair NULL or neither; at least one
+ *        pair is required). Configuration 2 alone always runs the separate
+ *        dK/dQ kernels and needs no workspace.
  *   workspace: ws_bytes >= streamkl_bwd_workspace_size(..., want_grad1) (may be
  *        NULL when that is 0); the call clears the part it uses (stream-ordered).
  */

@@ -110,6 +110,19 @@ def test_backward_validation(lib):
 
     assert bwd(0x1000, 0) == 1  # dq1 without dk1
     assert bwd(0, 0x1000) == 1
+
+    def bwd_sets(dq2, dk2, dq1, dk1):
+        f = lambda v: P(v) if v else None
+        return lib.streamkl_bwd(a, a, a, a, 1, 1, 8, 8, 64, 0.125, 0, a, a, a, a, f(dq2), f(dk2),
+                                f(dq1), f(dk1), None, 0, None, None)
+
+    assert bwd_sets(0, 0, 0, 0) == 1  # no gradient at all
+    assert b"no gradient" in lib.streamkl_last_error()
+    assert bwd_sets(0x1000, 0, 0x1000, 0x1000) == 1  # dq2 without dk2
+    # configuration 2 alone passes the gradient checks and fails only on the
+    # missing status word (checked last)
+    assert bwd_sets(0, 0, 0x1000, 0x1000) == 1
+    assert b"dev_status" in lib.streamkl_last_error()
     try:
         lib.streamkl_set_bwd_algorithm(1)  # the fused algorithm needs a workspace
         assert bwd(0, 0, ws=0) == 1

@@ -139,6 +139,34 @@ def test_ragged_shapes_one_gradient_set(NQ, NK, d, causal, algo):
     full_check(w, seed=NQ * 3 + NK, grad1=False, algo=algo)
 
 
+@pytest.mark.parametrize("NQ,NK,d,causal", [(256, 256, 64, False), (200, 333, 128, True),
+                                             (130, 131, 64, True)])
+def test_configuration2_only(NQ, NK, d, causal):
+    """dQ1/dK1 alone (P2 fixed, gist.science "Configuracion 2"): same values as
+    the oracle's configuration-2 gradients and as a run with both sets."""
+    w = synthetic.custom(f"cfg2_{NQ}x{NK}d{d}", B=2, H=3, NQ=NQ, NK=NK, d=d, causal=causal,
+                         noise=0.5, grad1=True)
+    dev = torch.device("cuda")
+    ins = synthetic.make_inputs(w, 7, dev)
+    q1, k1, q2, k2, g = ins
+    status = binding.new_status(dev)
+    kl, lse1, lse2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, dev_status=status)
+    only = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal, grad1=True,
+                                grad2=False, dev_status=status)
+    both = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal, grad1=True,
+                                dev_status=status)
+    binding.raise_on_device_status(status, "configuration 2 only")
+    assert only[0] is None and only[1] is None
+    assert torch.equal(only[2], both[2]) and torch.equal(only[3], both[3])
+    for b in range(w.B):
+        for hh in range(w.H):
+            h = [host(t[b, hh]) for t in ins[:4]]
+            og = orc.head_backward(*h, w.scale, w.causal, g[b, hh].cpu().numpy().astype(np.float64),
+                                   True)
+            assert_grad(host(only[2][b, hh]), og[2], "dq1")
+            assert_grad(host(only[3][b, hh]), og[3], "dk1")
+
+
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("d", [64, 128])
 def test_peaked_teacher_independent_student(d, algo):
