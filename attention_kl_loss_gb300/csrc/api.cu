@@ -92,29 +92,43 @@ streamkl_status check_sizes(int B, int H, int NQ, int NK, int d, int causal) {
 
 int key_tiles(int NK) { return (NK + skl::kBlockN - 1) / skl::kBlockN; }
 
-// Choose the split count by a wave model: time ~ waves * tiles per split.
-int choose_splits_impl(int B, int H, int NQ, int NK) {
+// Choose the split count with a two-part model of the forward's time:
+//   compute: waves of CTAs, each costing its key tiles plus a fixed start and
+//            end (Q load, TMEM set-up, partial-state write), one CTA per SM;
+//   memory:  the K1/K2 (and Q1/Q2) bytes over the HBM bandwidth, which one
+//            SM cannot reach alone: a few CTAs stream at ~100 GB/s each.
+// Splitting the keys adds CTAs (better SM fill, more streams) but cannot
+// beat the chip's bandwidth; with few query rows against many keys the
+// forward is memory-bound and splits only add partial-state traffic. The
+// constants are GB300 measurements: ~1 us per 128x128 tile pair at d = 128
+// (0.6 us at d = 64), ~3 us of fixed cost per CTA, ~7 TB/s of HBM bandwidth.
+int choose_splits_impl(int B, int H, int NQ, int NK, int d) {
   const long long ctas = static_cast<long long>((NQ + skl::kBlockM - 1) / skl::kBlockM) * B * H;
   const int tiles = key_tiles(NK);
   const int sms = num_sms();
   if (ctas >= 8LL * sms) return 1;
+  const double tile_us = d == 128 ? 1.0 : 0.6, cta_us = 3.0;
+  const double bytes = static_cast<double>(B) * H * (static_cast<double>(NK) + NQ) * d * 4.0;
   const int smax = std::max(1, std::min(32, tiles / 4));
   auto cost = [&](int s) {
     const long long units = ctas * s;
     const long long waves = (units + sms - 1) / sms;
     const long long tps = (tiles + s - 1) / s;
-    return waves * tps;
+    const double t_mma = static_cast<double>(waves) * (static_cast<double>(tps) * tile_us + cta_us);
+    const double streams = static_cast<double>(std::min<long long>(units, sms));
+    const double t_mem = bytes / std::min(7.0e12, streams * 1.0e11) * 1e6;
+    return std::max(t_mma, t_mem);
   };
   int best = 1;
-  long long best_t = cost(1);
+  double best_t = cost(1);
   for (int s = 2; s <= smax; ++s) {
-    const long long t = cost(s);
+    const double t = cost(s);
     if (t < best_t) {
       best_t = t;
       best = s;
     }
   }
-  if (best > 1 && static_cast<double>(best_t) > 0.95 * static_cast<double>(cost(1))) return 1;
+  if (best > 1 && best_t > 0.95 * cost(1)) return 1;
   return best;
 }
 
@@ -146,11 +160,18 @@ int forced_algo() {
   return v;
 }
 
-int bwd_algo_impl(int B, int H, int NQ, int NK) {
+// Automatic choice, from the fused-vs-separate sweep on GB300: the separate
+// kernels win everywhere except configuration 1 alone with a short query
+// range against a long key range (129..512 query rows, at least 128 keys per
+// query row, d = 128), where the fused kernel's single pass over the keys is
+// ~3 % faster; the dK kernel then has many key blocks with only a few query
+// steps each.
+int bwd_algo_impl(int B, int H, int NQ, int NK, int d, int grad1) {
   const int forced = forced_algo();
   if (forced >= 0) return forced;
-  (void)B, (void)H, (void)NQ, (void)NK;
-  return 0;
+  (void)B, (void)H;
+  const bool fused = d == 128 && !grad1 && NQ > 128 && NQ <= 512 && NK >= 128LL * NQ;
+  return fused ? 1 : 0;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -161,7 +182,7 @@ size_t fwd_ws(int B, int H, int NQ, int splits) {
 }
 
 size_t bwd_ws(int B, int H, int NQ, int NK, int d, int grad1) {
-  if (bwd_algo_impl(B, H, NQ, NK) == 0) return 0;
+  if (bwd_algo_impl(B, H, NQ, NK, d, grad1) == 0) return 0;
   const size_t one = align256(static_cast<size_t>(B) * H * NQ * d * sizeof(float));
   return grad1 ? 2 * one : one;
 }
@@ -214,14 +235,14 @@ const char* streamkl_last_error(void) { return g_err; }
 int streamkl_choose_splits(int B, int H, int NQ, int NK, int d, int causal) {
   if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return 0;
   int s, tps;
-  split_plan(choose_splits_impl(B, H, NQ, NK), NK, &s, &tps);
+  split_plan(choose_splits_impl(B, H, NQ, NK, d), NK, &s, &tps);
   return s;
 }
 
 size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal, int num_splits) {
   if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK || num_splits < 0) return 0;
   int s, tps;
-  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK), NK, &s, &tps);
+  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK, d), NK, &s, &tps);
   return fwd_ws(B, H, NQ, s);
 }
 
@@ -231,9 +252,8 @@ size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int caus
 }
 
 int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
-  (void)want_grad1;
   if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return -1;
-  return bwd_algo_impl(B, H, NQ, NK);
+  return bwd_algo_impl(B, H, NQ, NK, d, want_grad1 ? 1 : 0);
 }
 
 int streamkl_set_bwd_algorithm(int algo) {
@@ -265,7 +285,7 @@ streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, con
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(STREAMKL_ERR_INVALID_ARG, "scale must be finite and > 0");
   if (num_splits < 0) return fail(STREAMKL_ERR_INVALID_ARG, "num_splits must be >= 0");
   int splits, tps;
-  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK), NK, &splits, &tps);
+  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK, d), NK, &splits, &tps);
   const size_t need = fwd_ws(B, H, NQ, splits);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
     return fail(STREAMKL_ERR_INVALID_ARG, "forward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
@@ -358,7 +378,7 @@ streamkl_status streamkl_fwd_noalloc(const void* q1, const void* k1, const void*
   if (st != STREAMKL_OK) return st;
   if (num_splits < 0) return fail(STREAMKL_ERR_INVALID_ARG, "num_splits must be >= 0");
   int splits, tps;
-  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK), NK, &splits, &tps);
+  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK, d), NK, &splits, &tps);
   const size_t need = fwd_ws(B, H, NQ, splits);
   if (need > kFwdScratchBytes)
     return fail(STREAMKL_ERR_INVALID_ARG,
@@ -393,7 +413,7 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   const int grad1 = dq1 != nullptr, grad2 = dq2 != nullptr;
   // configuration 2 alone always runs the separate kernels (the fused kernel
   // always produces dQ2/dK2)
-  const int algo = grad2 ? bwd_algo_impl(B, H, NQ, NK) : 0;
+  const int algo = grad2 ? bwd_algo_impl(B, H, NQ, NK, d, grad1) : 0;
   const size_t need = algo == 0 ? 0 : bwd_ws(B, H, NQ, NK, d, grad1);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
     return fail(STREAMKL_ERR_INVALID_ARG, "backward workspace too small: need %zu bytes, got %zu", need, ws_bytes);

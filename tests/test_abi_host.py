@@ -43,20 +43,27 @@ def test_status_strings(lib):
 
 
 def test_split_choice(lib):
-    # 128 (b,h) x 4 query tiles over 1024 key tiles: 8 splits fill 152 SMs
-    assert lib.streamkl_choose_splits(4, 32, 512, 131072, 128, 1) == 8
+    # 128 (b,h) x 4 query tiles over 1024 key tiles: compute-bound, 3.4 waves
+    # without a split; splitting the keys evens out the last wave
+    assert lib.streamkl_choose_splits(4, 32, 512, 131072, 128, 1) > 1
     # plenty of query tiles: no split
     assert lib.streamkl_choose_splits(1, 32, 65536, 65536, 128, 1) == 1
     assert lib.streamkl_choose_splits(2, 16, 4096, 4096, 128, 0) == 1
     assert lib.streamkl_choose_splits(1, 8, 16384, 16384, 64, 0) == 1
-    # decode-like single row: split the keys
-    assert lib.streamkl_choose_splits(1, 32, 1, 65536, 128, 1) > 4
+    # one query row, 32 heads: 32 CTAs cannot stream K at full bandwidth, so
+    # the keys are split across more SMs
+    assert lib.streamkl_choose_splits(1, 32, 1, 65536, 128, 1) > 1
+    # few query rows over 128 heads: already memory-bound with one CTA per
+    # head (measured: splits 0.95-1.00x), so no split
+    assert lib.streamkl_choose_splits(4, 32, 1, 65536, 128, 1) == 1
+    assert lib.streamkl_choose_splits(4, 32, 64, 65536, 128, 1) == 1
     # invalid sizes
     assert lib.streamkl_choose_splits(1, 1, 8, 4, 64, 1) == 0
 
 
 def test_workspace_sizes(lib):
-    assert lib.streamkl_fwd_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 5 * 8 * 128 * 512 * 4
+    s = lib.streamkl_choose_splits(4, 32, 512, 131072, 128, 1)
+    assert lib.streamkl_fwd_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 5 * s * 128 * 512 * 4
     assert lib.streamkl_fwd_workspace_size(4, 32, 512, 131072, 128, 1, 1) == 0
     try:
         assert lib.streamkl_set_bwd_algorithm(1) == 0  # fused: fp32 dQ accumulators
@@ -64,14 +71,29 @@ def test_workspace_sizes(lib):
         assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 1) == 2 * 32 * 65536 * 128 * 4
         assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 0) == 32 * 65536 * 128 * 4
         assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == max(
-            5 * 8 * 128 * 512 * 4, 128 * 512 * 128 * 4)
+            5 * s * 128 * 512 * 4, 128 * 512 * 128 * 4)
         assert lib.streamkl_set_bwd_algorithm(0) == 0  # separate: no workspace
         assert lib.streamkl_bwd_algorithm(1, 32, 65536, 65536, 128, 1, 1) == 0
         assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 1) == 0
-        assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 5 * 8 * 128 * 512 * 4
+        assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 5 * s * 128 * 512 * 4
         assert lib.streamkl_set_bwd_algorithm(7) == -1
     finally:
         lib.streamkl_set_bwd_algorithm(-1)
+
+
+def test_automatic_backward_choice(lib):
+    lib.streamkl_set_bwd_algorithm(-1)
+    # separate kernels by default
+    assert lib.streamkl_bwd_algorithm(1, 32, 65536, 65536, 128, 1, 1) == 0
+    assert lib.streamkl_bwd_algorithm(4, 32, 64, 65536, 128, 1, 0) == 0
+    assert lib.streamkl_bwd_algorithm(4, 32, 1024, 131072, 128, 1, 0) == 0
+    # fused: configuration 1 alone, short query range over many keys, d = 128
+    assert lib.streamkl_bwd_algorithm(4, 32, 512, 131072, 128, 1, 0) == 1
+    assert lib.streamkl_bwd_algorithm(4, 32, 256, 65536, 128, 1, 0) == 1
+    assert lib.streamkl_bwd_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 4 * 32 * 512 * 128 * 4
+    # ... but not with both gradient sets or at d = 64
+    assert lib.streamkl_bwd_algorithm(4, 32, 512, 131072, 128, 1, 1) == 0
+    assert lib.streamkl_bwd_algorithm(4, 32, 512, 131072, 64, 1, 0) == 0
 
 
 def test_forced_split_workspace_rounding(lib):
