@@ -69,6 +69,10 @@ WORKLOADS = {
         # profiler captures (256 MiB of inputs: above L2, a few GB at most)
         Workload("causal16k_profile", B=1, H=16, NQ=16384, NK=16384, d=128, causal=True,
                  noise=0.2, grad1=True),
+        # the 64K causal shape on 4 heads: DRAM-traffic captures, whose per-head
+        # traffic and work are those of the full 32-head workload
+        Workload("causal64k_h4", B=1, H=4, NQ=65536, NK=65536, d=128, causal=True, noise=0.2,
+                 grad1=True),
     ]
 }
 

@@ -263,6 +263,30 @@ def reference_arm(args, w):
     return 0
 
 
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture
+    (profiles/dram_traffic.json), or None when there is none for this workload
+    or the kernel's sources have changed since it was taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            doc = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in doc.get("entries", []):
+        if e.get("workload") != workload or e.get("kernel") != kernel:
+            continue
+        h = hashlib.sha256()
+        try:
+            for src in e["sources"]:
+                with open(os.path.join(ROOT, src), "rb") as f:
+                    h.update(f.read())
+        except OSError:
+            return None
+        return float(e["bytes_per_launch"]) if h.hexdigest() == e.get("sha256") else None
+    return None
+
+
 def describe(w):
     return (f"{w.name}: B={w.B} H={w.H} N_Q={w.NQ} N_K={w.NK} d={w.d} "
             f"{'causal' if w.causal else 'non-causal'}, bf16 inputs, fwd+bwd"
@@ -354,7 +378,8 @@ def gpu_arm(args, w):
     dom = bwd_name if bwd_ms >= fwd_ms else "streamkl_fwd_kernel"
     dom_tf = kernels[dom]["achieved_tflops"]
     roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": sustained,
-                "unit": "TFLOP/s", "frac": dom_tf / sustained, "traffic": None,
+                "unit": "TFLOP/s", "frac": dom_tf / sustained,
+                "traffic": recorded_traffic(w.name, dom),
                 "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a long step)"}
     if algo == binding.BWD_SEPARATE:
         launches_per_step = 1 + (1 if splits > 1 else 0) + 2
