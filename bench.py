@@ -351,6 +351,7 @@ def gpu_arm(args, w):
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
 
     f_fwd, f_bwd_metric, f_bwd_work, f_fwd_exact, f_bwd_exact = flop_counts(w)
+    f_bwd_work_exact = f_bwd_exact
     algo = binding.bwd_algorithm(B, H, NQ, NK, d, w.causal, w.grad1)
     pairs = w.live_pairs_per_head() * B * H
     if algo == binding.BWD_SEPARATE:
@@ -415,6 +416,13 @@ def gpu_arm(args, w):
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
             "bwd_tflops_metric": f_bwd_metric / (bwd_ms * 1e-3) / 1e12,
+            # the same times over exact counts: visible (query, key) pairs,
+            # 4d FLOPs per pair forward, 8d (one gradient set) or 12d (both)
+            # backward, i.e. the work the method needs, not what one kernel
+            # design executes
+            "visible_pairs": pairs,
+            "fwd_tflops_exact": f_fwd_exact / (fwd_ms * 1e-3) / 1e12,
+            "bwd_tflops_work": f_bwd_work_exact / (bwd_ms * 1e-3) / 1e12,
             "pct_of_measured_peak": {"value": value / world / pk["bf16_tflops"],
                                      "fwd": f_fwd / (fwd_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
                                      "bwd_metric": f_bwd_metric / (bwd_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
