@@ -45,6 +45,10 @@ _SIGNATURES = {
     "streamkl_set_bwd_algorithm": (_I, [_I]),
     "streamkl_fwd_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P,
                                   _P, _P]),
+    "streamkl_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                 _P, _P, _P, _P, _P]),
+    "streamkl_bwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
+                                 _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -224,6 +228,77 @@ def streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = N
                           _ptr(dk2), _ptr(dq1), _ptr(dk1), _ptr(ws), need, _ptr(status),
                           _stream_handle(stream))
     _check(st, "streamkl_bwd")
+    return dq2, dk2, dq1, dk1
+
+
+def _packed_dims(q1, k1, q2, k2, cu_seqlens_q, cu_seqlens_k):
+    for name, t in (("q1", q1), ("k1", k1), ("q2", q2), ("k2", k2)):
+        if not isinstance(t, torch.Tensor) or t.dim() != 3:
+            raise ValueError(f"{name} must be a 3-D packed tensor [total, H, d]")
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    TQ, H, d = q1.shape
+    TK = k1.shape[0]
+    if q2.shape != q1.shape or k1.shape != (TK, H, d) or k2.shape != k1.shape:
+        raise ValueError("shape mismatch: Q1,Q2 must be [total_q,H,d] and K1,K2 [total_k,H,d]")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if t.dtype != torch.int32 or not t.is_cuda or t.dim() != 1 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA vector [B + 1]")
+    if cu_seqlens_k.numel() != cu_seqlens_q.numel() or cu_seqlens_q.numel() < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B + 1 >= 2 entries")
+    return cu_seqlens_q.numel() - 1, H, TQ, TK, d
+
+
+def streamkl_fwd_varlen(q1, k1, q2, k2, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                        max_seqlen_k: int, scale: Optional[float] = None, causal: bool = False,
+                        out=None, dev_status=None, stream=None):
+    """Forward for a packed variable-length batch: q1/q2 [total_q, H, d],
+    k1/k2 [total_k, H, d] bf16, cu_seqlens_* int32 device offsets [B + 1].
+    Returns (kl, lse1, lse2), fp32 [total_q, H]."""
+    lib = load()
+    B, H, TQ, TK, d = _packed_dims(q1, k1, q2, k2, cu_seqlens_q, cu_seqlens_k)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dev = q1.device
+    if out is None:
+        out = tuple(torch.empty((TQ, H), dtype=torch.float32, device=dev) for _ in range(3))
+    kl, lse1, lse2 = out
+    status = dev_status if dev_status is not None else new_status(dev)
+    st = lib.streamkl_fwd_varlen(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(cu_seqlens_q),
+                                 _ptr(cu_seqlens_k), B, H, TQ, TK, int(max_seqlen_q),
+                                 int(max_seqlen_k), d, scale, int(causal), _ptr(kl), _ptr(lse1),
+                                 _ptr(lse2), _ptr(status), _stream_handle(stream))
+    _check(st, "streamkl_fwd_varlen")
+    return kl, lse1, lse2
+
+
+def streamkl_bwd_varlen(q1, k1, q2, k2, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                        max_seqlen_k: int, kl, lse1, lse2, dkl, scale: Optional[float] = None,
+                        causal: bool = False, grad1: bool = False, grad2: bool = True, out=None,
+                        dev_status=None, stream=None):
+    """Backward for a packed variable-length batch; returns (dq2, dk2, dq1,
+    dk1) shaped like the inputs, None where not requested."""
+    if not (grad1 or grad2):
+        raise ValueError("no gradient requested (grad1 and grad2 both False)")
+    lib = load()
+    B, H, TQ, TK, d = _packed_dims(q1, k1, q2, k2, cu_seqlens_q, cu_seqlens_k)
+    for name, t in (("kl", kl), ("lse1", lse1), ("lse2", lse2), ("dkl", dkl)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.shape != (TQ, H):
+            raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor [total_q, H]")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        dq2 = torch.empty_like(q2) if grad2 else None
+        dk2 = torch.empty_like(k2) if grad2 else None
+        dq1 = torch.empty_like(q1) if grad1 else None
+        dk1 = torch.empty_like(k1) if grad1 else None
+    else:
+        dq2, dk2, dq1, dk1 = out
+    status = dev_status if dev_status is not None else new_status(q1.device)
+    st = lib.streamkl_bwd_varlen(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(cu_seqlens_q),
+                                 _ptr(cu_seqlens_k), B, H, TQ, TK, int(max_seqlen_q),
+                                 int(max_seqlen_k), d, scale, int(causal), _ptr(kl), _ptr(lse1),
+                                 _ptr(lse2), _ptr(dkl), _ptr(dq2), _ptr(dk2), _ptr(dq1), _ptr(dk1),
+                                 _ptr(status), _stream_handle(stream))
+    _check(st, "streamkl_bwd_varlen")
     return dq2, dk2, dq1, dk1
 
 

@@ -205,6 +205,42 @@ streamkl_status make_map(CUtensorMap* m, const void* ptr, int BH, int N, int d, 
   return STREAMKL_OK;
 }
 
+// 3-D map {d, total, H} of a packed [total, H, d] bf16 tensor: rows of one
+// head are H d elements apart. 64-column x box_rows boxes, 128-byte swizzle.
+streamkl_status make_map_packed(CUtensorMap* m, const void* ptr, int total, int H, int d,
+                                const char* name, int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return fail(STREAMKL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(total),
+                              static_cast<cuuint64_t>(H)};
+  const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(H) * d * 2, static_cast<cuuint64_t>(d) * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), gdim, gstride, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(STREAMKL_ERR_CUDA, "tensor map for %s failed (CUresult %d)", name, static_cast<int>(r));
+  return STREAMKL_OK;
+}
+
+// Host checks shared by the packed entry points (the offsets themselves are
+// device data: the kernels check them and report STREAMKL_ERR_INVALID_ARG
+// through the status word).
+streamkl_status check_packed(const int* cu_q, const int* cu_k, int B, int H, int total_q, int total_k,
+                             int max_q, int max_k, int d, int causal) {
+  if (!cu_q || !cu_k) return fail(STREAMKL_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k must be non-NULL");
+  if ((reinterpret_cast<uintptr_t>(cu_q) | reinterpret_cast<uintptr_t>(cu_k)) & 3)
+    return fail(STREAMKL_ERR_INVALID_ARG, "cu_seqlens arrays must be 4-byte aligned");
+  if (total_q < 1 || total_k < 1) return fail(STREAMKL_ERR_INVALID_ARG, "total_q and total_k must be >= 1");
+  if (max_q > total_q || max_k > total_k)
+    return fail(STREAMKL_ERR_INVALID_ARG, "max_seqlen above the packed total (%d > %d or %d > %d)",
+                max_q, total_q, max_k, total_k);
+  if (static_cast<long long>(total_q) * H > (1LL << 31) || static_cast<long long>(total_k) * H > (1LL << 31))
+    return fail(STREAMKL_ERR_UNSUPPORTED, "total rows x heads above 2^31");
+  // the per-sequence causal condition (N_Q <= N_K) is checked on the device
+  return check_sizes(B, H, max_q, max_k, d, 0);
+}
+
 streamkl_status check_inputs(const void* q1, const void* k1, const void* q2, const void* k2) {
   const void* ps[4] = {q1, k1, q2, k2};
   const char* names[4] = {"q1", "k1", "q2", "k2"};
@@ -303,6 +339,7 @@ streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, con
   a.tm_q2 = &mq2;
   a.tm_k2 = &mk2;
   a.BH = BH;
+  a.plane = static_cast<long long>(BH) * NQ;
   a.NQ = NQ;
   a.NK = NK;
   a.d = d;
@@ -490,6 +527,116 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
     e = skl::launch_dq_convert(a.dq1acc, dq1, n, s);
     if (e != cudaSuccess) return cuda_fail(e, "dq1 convert launch");
   }
+  return STREAMKL_OK;
+}
+
+streamkl_status streamkl_fwd_varlen(const void* q1, const void* k1, const void* q2, const void* k2,
+                                    const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                                    int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                                    int d, float scale, int causal, float* kl, float* lse1,
+                                    float* lse2, int* dev_status, void* stream) {
+  g_err[0] = '\0';
+  streamkl_status st = check_packed(cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k,
+                                    max_seqlen_q, max_seqlen_k, d, causal);
+  if (st != STREAMKL_OK) return st;
+  if (causal != 0 && causal != 1) return fail(STREAMKL_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if ((st = check_inputs(q1, k1, q2, k2)) != STREAMKL_OK) return st;
+  if (!kl || !lse1 || !lse2) return fail(STREAMKL_ERR_INVALID_ARG, "kl, lse1, lse2 must be non-NULL");
+  if (!dev_status) return fail(STREAMKL_ERR_INVALID_ARG, "dev_status must be non-NULL");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(STREAMKL_ERR_INVALID_ARG, "scale must be finite and > 0");
+  CUtensorMap mq1, mk1, mq2, mk2;
+  if ((st = make_map_packed(&mq1, q1, total_q, H, d, "q1", skl::kBlockM)) != STREAMKL_OK) return st;
+  if ((st = make_map_packed(&mk1, k1, total_k, H, d, "k1", skl::kBlockM)) != STREAMKL_OK) return st;
+  if ((st = make_map_packed(&mq2, q2, total_q, H, d, "q2", skl::kBlockM)) != STREAMKL_OK) return st;
+  if ((st = make_map_packed(&mk2, k2, total_k, H, d, "k2", skl::kBlockM)) != STREAMKL_OK) return st;
+  skl::FwdArgs a{};
+  a.tm_q1 = &mq1;
+  a.tm_k1 = &mk1;
+  a.tm_q2 = &mq2;
+  a.tm_k2 = &mk2;
+  a.BH = B * H;
+  a.NQ = max_seqlen_q;
+  a.NK = max_seqlen_k;
+  a.d = d;
+  a.causal = causal;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.H = H;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.plane = static_cast<long long>(total_q) * H;
+  a.scale = scale;
+  a.kl = kl;
+  a.lse1 = lse1;
+  a.lse2 = lse2;
+  a.part = nullptr;
+  a.splits = 1;
+  a.tiles_per_split = key_tiles(max_seqlen_k);
+  a.dev_status = dev_status;
+  a.timeout_ns = wait_timeout_ns();
+  cudaError_t e = skl::launch_fwd(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return STREAMKL_OK;
+}
+
+streamkl_status streamkl_bwd_varlen(const void* q1, const void* k1, const void* q2, const void* k2,
+                                    const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                                    int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                                    int d, float scale, int causal, const float* kl,
+                                    const float* lse1, const float* lse2, const float* dkl,
+                                    void* dq2, void* dk2, void* dq1, void* dk1, int* dev_status,
+                                    void* stream) {
+  g_err[0] = '\0';
+  streamkl_status st = check_packed(cu_seqlens_q, cu_seqlens_k, B, H, total_q, total_k,
+                                    max_seqlen_q, max_seqlen_k, d, causal);
+  if (st != STREAMKL_OK) return st;
+  if (causal != 0 && causal != 1) return fail(STREAMKL_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if ((st = check_inputs(q1, k1, q2, k2)) != STREAMKL_OK) return st;
+  if (!kl || !lse1 || !lse2 || !dkl) return fail(STREAMKL_ERR_INVALID_ARG, "kl/lse1/lse2/dkl must be non-NULL");
+  if ((dq2 == nullptr) != (dk2 == nullptr))
+    return fail(STREAMKL_ERR_INVALID_ARG, "dq2 and dk2 must be both NULL or both non-NULL");
+  if ((dq1 == nullptr) != (dk1 == nullptr))
+    return fail(STREAMKL_ERR_INVALID_ARG, "dq1 and dk1 must be both NULL or both non-NULL");
+  if (!dq2 && !dq1) return fail(STREAMKL_ERR_INVALID_ARG, "no gradient requested: dq2/dk2 and dq1/dk1 are all NULL");
+  if ((dq2 && (!aligned16(dq2) || !aligned16(dk2))) || (dq1 && (!aligned16(dq1) || !aligned16(dk1))))
+    return fail(STREAMKL_ERR_INVALID_ARG, "gradient outputs must be 16-byte aligned");
+  if (!dev_status) return fail(STREAMKL_ERR_INVALID_ARG, "dev_status must be non-NULL");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(STREAMKL_ERR_INVALID_ARG, "scale must be finite and > 0");
+  CUtensorMap mq1, mk1, mq2, mk2;  // the separate kernels move 64-row boxes
+  if ((st = make_map_packed(&mq1, q1, total_q, H, d, "q1", 64)) != STREAMKL_OK) return st;
+  if ((st = make_map_packed(&mk1, k1, total_k, H, d, "k1", 64)) != STREAMKL_OK) return st;
+  if ((st = make_map_packed(&mq2, q2, total_q, H, d, "q2", 64)) != STREAMKL_OK) return st;
+  if ((st = make_map_packed(&mk2, k2, total_k, H, d, "k2", 64)) != STREAMKL_OK) return st;
+  skl::BwdSepArgs a{};
+  a.tm_q1 = &mq1;
+  a.tm_k1 = &mk1;
+  a.tm_q2 = &mq2;
+  a.tm_k2 = &mk2;
+  a.BH = B * H;
+  a.NQ = max_seqlen_q;
+  a.NK = max_seqlen_k;
+  a.d = d;
+  a.causal = causal;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.H = H;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.grad1 = dq1 != nullptr;
+  a.grad2 = dq2 != nullptr;
+  a.scale = scale;
+  a.kl = kl;
+  a.lse1 = lse1;
+  a.lse2 = lse2;
+  a.g = dkl;
+  a.dq2 = dq2;
+  a.dk2 = dk2;
+  a.dq1 = dq1;
+  a.dk1 = dk1;
+  a.dev_status = dev_status;
+  a.timeout_ns = wait_timeout_ns();
+  cudaError_t e = skl::launch_bwd_separate(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return STREAMKL_OK;
 }
 

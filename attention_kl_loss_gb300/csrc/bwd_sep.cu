@@ -97,7 +97,10 @@ __device__ __forceinline__ float4 query_const(const float* lse1, const float* ls
   return q;
 }
 
-template <int D, bool DQ, int SETS>
+// PACKED: a variable-length batch of packed sequences instead of dense
+// [B, H, N, d] tensors; a template parameter so that the dense kernel keeps
+// its sizes as kernel parameters.
+template <int D, bool DQ, int SETS, bool PACKED>
 __global__ void __launch_bounds__(kSepThreads, 1)
     streamkl_bwd_sep_kernel(const __grid_constant__ CUtensorMap tm_x1,
                             const __grid_constant__ CUtensorMap tm_x2,
@@ -106,8 +109,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
                             int causal, float scale, const float* __restrict__ kl_in,
                             const float* __restrict__ lse1_in, const float* __restrict__ lse2_in,
                             const float* __restrict__ g_in, __nv_bfloat16* __restrict__ out2,
-                            __nv_bfloat16* __restrict__ out1, int* dev_status,
-                            uint64_t timeout_ns) {
+                            __nv_bfloat16* __restrict__ out1, const int* __restrict__ cu_q,
+                            const int* __restrict__ cu_k, int H, int total_q, int total_k,
+                            int* dev_status, uint64_t timeout_ns) {
   using L = SepLayout<D, DQ, SETS>;
   constexpr bool HAS2 = SETS & kSet2, HAS1 = SETS & kSet1;
   extern __shared__ uint8_t smem_raw[];
@@ -116,24 +120,31 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   uint8_t* gb = smem_raw + (sb - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int NX = DQ ? NQ : NK;
+  const int bh = static_cast<int>(blockIdx.y);
+  // this (batch, head) slice: the whole tensor's sizes, or one sequence of a
+  // packed variable-length batch (the grid covers the longest one)
+  const SeqView sv = PACKED ? seq_view_packed(bh, H, NQ, NK, D, cu_q, cu_k, total_q, total_k)
+                            : seq_view_dense(bh, NQ, NK, D);
+  const int nq = sv.nq, nk = sv.nk;
+  const int NX = DQ ? nq : nk;
   const int nxb = (NX + kBlockM - 1) / kBlockM;
-  const int off = NK - NQ;  // key j is visible to query i iff j <= i + off (causal)
+  const bool active = sv.ok && static_cast<int>(blockIdx.x) < nxb && !(causal && nq > nk);
+  const int off = nk - nq;  // key j is visible to query i iff j <= i + off (causal)
   // causal: the dQ kernel's heavy blocks are the last query blocks, the dK
   // kernel's the first key blocks; launch the heavy ones first
   const int xb = (DQ && causal) ? nxb - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int bh = static_cast<int>(blockIdx.y);
   const int x0 = xb * kBlockM;
+  const int x_row0 = DQ ? sv.q_row0 : sv.k_row0, y_row0 = DQ ? sv.k_row0 : sv.q_row0;
   int y_begin, y_end;  // in steps of 64 Y rows
   if (DQ) {  // key steps visible to some row of this query block
-    const int klim = causal ? min(NK, min(NQ, x0 + kBlockM) + off) : NK;
+    const int klim = causal ? min(nk, min(nq, x0 + kBlockM) + off) : nk;
     y_begin = 0;
     y_end = (klim + kStepRows - 1) / kStepRows;
   } else {  // query steps with a row that sees some key of this block
     y_begin = causal ? max(0, x0 - off) / kStepRows : 0;
-    y_end = (NQ + kStepRows - 1) / kStepRows;
+    y_end = (nq + kStepRows - 1) / kStepRows;
   }
-  int n_iter = y_end - y_begin;
+  int n_iter = active ? y_end - y_begin : 0;
 
   const uint32_t bar0 = sb + L::OFF_BAR;
   const uint32_t x_full = bar0;
@@ -173,6 +184,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     *abort_flag = 0;
     // a failure recorded earlier (this launch or a previous one) skips the work
     *skip_flag = *reinterpret_cast<volatile int*>(dev_status) != 0;
+    // malformed sequence offsets, or a causal sequence with more query rows
+    // than keys: reported, never computed
+    if (!sv.ok || (causal && nq > nk)) atomicCAS(dev_status, 0, kStatusInvalidArg);
     *t_queued = 0;
     fence_mbar_init();
   }
@@ -205,18 +219,20 @@ __global__ void __launch_bounds__(kSepThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               tma_load_3d(sb + L::OFF_X + t * L::XT + b * 16384 + h * 8192, t == 0 ? &tm_x1 : &tm_x2,
-                          x_full, b * 64, x0 + h * kStepRows, bh);
+                          x_full, b * 64, x_row0 + x0 + h * kStepRows, sv.z);
       }
-      const size_t qbase = static_cast<size_t>(bh) * NQ;
+      auto qv = [&](int q) {  // per-row vector element of query row q
+        return static_cast<size_t>(sv.v_off + static_cast<long long>(q) * sv.v_stride);
+      };
       int it = 0;
       for (; it < n_iter; ++it) {
         const int s = it % kStages;
         const int yrow = (y_begin + it) * kStepRows;
         float4 c0, c1;  // dK kernel: this lane's two table entries, loaded before the wait
         if (!DQ) {
-          c0 = query_const(lse1_in, lse2_in, g_in, kl_in, qbase + yrow + lane, scale, yrow + lane < NQ);
-          c1 = query_const(lse1_in, lse2_in, g_in, kl_in, qbase + yrow + lane + 32, scale,
-                           yrow + lane + 32 < NQ);
+          c0 = query_const(lse1_in, lse2_in, g_in, kl_in, qv(yrow + lane), scale, yrow + lane < nq);
+          c1 = query_const(lse1_in, lse2_in, g_in, kl_in, qv(yrow + lane + 32), scale,
+                           yrow + lane + 32 < nq);
         }
         bool good = true;
         if (lane == 0) good = wait_bounded(y_empty(s), ((it / kStages) & 1) ^ 1, wc);
@@ -237,7 +253,7 @@ __global__ void __launch_bounds__(kSepThreads, 1)
 #pragma unroll
             for (int b = 0; b < L::KB; ++b)
               tma_load_3d(dst + t * L::YT + b * 8192, t == 0 ? &tm_y1 : &tm_y2, y_full(s), b * 64,
-                          yrow, bh);
+                          y_row0 + yrow, sv.z);
         }
       }
       // let every copy this thread issued land before the CTA can exit
@@ -338,8 +354,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     // dQ kernel: constants of this thread's query row
     float4 rc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (DQ)
-      rc = query_const(lse1_in, lse2_in, g_in, kl_in, static_cast<size_t>(bh) * NQ + xrow, scale,
-                       xrow < NQ);
+      rc = query_const(lse1_in, lse2_in, g_in, kl_in,
+                       static_cast<size_t>(sv.v_off + static_cast<long long>(xrow) * sv.v_stride),
+                       scale, xrow < nq);
 
     // T of step `it` into a, b (all lanes agree on every wait's outcome, so
     // the warp-wide TMEM loads and the __syncwarp below are never reached by
@@ -372,13 +389,13 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         bool full;
         int lim = 0;
         if (DQ) {
-          lim = causal ? min(NK, xrow + 1 + off) : NK;  // keys < lim visible
+          lim = causal ? min(nk, xrow + 1 + off) : nk;  // keys < lim visible
           full = y0 + 16 <= lim;
         } else {
           lim = causal ? xrow - off : 0;  // queries >= lim (and < N_Q) see this key
-          full = y0 + 16 <= NQ && y0 >= lim;
+          full = y0 + 16 <= nq && y0 >= lim;
         }
-        auto visible = [&](int y) { return DQ ? y < lim : (y < NQ && y >= lim); };
+        auto visible = [&](int y) { return DQ ? y < lim : (y < nq && y >= lim); };
         const float* tq = tab + (it % kStages) * 4 * kStepRows + grp * 16;
         const float2 c2 = make_float2(c, c), sc2 = make_float2(scale, scale);
         const float2 m1 = make_float2(-1.f, -1.f);
@@ -458,8 +475,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
           tmem_ld16(tmem + lane_off + L::COL_ACC + t * D + grp * EC, v);
         tmem_wait_ld();
         if (xrow < NX) {
-          uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * NX + xrow) * D +
-                                                grp * EC);
+          uint4* dst = reinterpret_cast<uint4*>(
+              out + (DQ ? sv.q_off : sv.k_off) + static_cast<long long>(xrow) * sv.row_stride +
+              grp * EC);
 #pragma unroll
           for (int i = 0; i < EC / 8; ++i)
             dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]),
@@ -479,13 +497,13 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   }
 }
 
-template <int D, bool DQ, int SETS>
-cudaError_t launch_sep_t(const BwdSepArgs& a, cudaStream_t stream) {
+template <int D, bool DQ, int SETS, bool PACKED>
+cudaError_t launch_sep_p(const BwdSepArgs& a, cudaStream_t stream) {
   using L = SepLayout<D, DQ, SETS>;
-  auto kern = streamkl_bwd_sep_kernel<D, DQ, SETS>;
+  auto kern = streamkl_bwd_sep_kernel<D, DQ, SETS, PACKED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
-  const int NX = DQ ? a.NQ : a.NK;
+  const int NX = DQ ? a.NQ : a.NK;  // the longest sequence for packed batches
   dim3 grid((NX + kBlockM - 1) / kBlockM, a.BH, 1);
   const CUtensorMap* x1 = DQ ? a.tm_q1 : a.tm_k1;
   const CUtensorMap* x2 = DQ ? a.tm_q2 : a.tm_k2;
@@ -494,8 +512,15 @@ cudaError_t launch_sep_t(const BwdSepArgs& a, cudaStream_t stream) {
   kern<<<grid, kSepThreads, L::ALLOC, stream>>>(
       *x1, *x2, *y1, *y2, a.NQ, a.NK, a.causal, a.scale, a.kl, a.lse1, a.lse2, a.g,
       static_cast<__nv_bfloat16*>(DQ ? a.dq2 : a.dk2),
-      static_cast<__nv_bfloat16*>(DQ ? a.dq1 : a.dk1), a.dev_status, a.timeout_ns);
+      static_cast<__nv_bfloat16*>(DQ ? a.dq1 : a.dk1), a.cu_q, a.cu_k, a.H, a.total_q, a.total_k,
+      a.dev_status, a.timeout_ns);
   return cudaGetLastError();
+}
+
+template <int D, bool DQ, int SETS>
+cudaError_t launch_sep_t(const BwdSepArgs& a, cudaStream_t stream) {
+  return a.cu_q != nullptr ? launch_sep_p<D, DQ, SETS, true>(a, stream)
+                           : launch_sep_p<D, DQ, SETS, false>(a, stream);
 }
 
 template <int D, bool DQ>

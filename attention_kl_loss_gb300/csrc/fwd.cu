@@ -143,7 +143,10 @@ __device__ __forceinline__ void finish_row(const RowState& s, float scale, float
   kl = scale * (s.acc / s.l1) - lse1 + lse2;
 }
 
-template <int D, bool SPLIT>
+// PACKED: a variable-length batch of packed sequences (no split-K) instead of
+// dense [B, H, N, d] tensors; a template parameter so that the dense kernel
+// keeps its sizes as kernel parameters.
+template <int D, bool SPLIT, bool PACKED>
 __global__ void __launch_bounds__(kFwdThreads, 1)
     streamkl_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1,
                         const __grid_constant__ CUtensorMap tm_k1,
@@ -151,7 +154,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                         const __grid_constant__ CUtensorMap tm_k2, int NQ, int NK, int causal,
                         float scale, float* __restrict__ kl_out, float* __restrict__ lse1_out,
                         float* __restrict__ lse2_out, float* __restrict__ part, int splits,
-                        int tiles_per_split, int BH, int* dev_status, uint64_t timeout_ns) {
+                        int tiles_per_split, long long plane, const int* __restrict__ cu_q,
+                        const int* __restrict__ cu_k, int H, int total_q, int total_k,
+                        int* dev_status, uint64_t timeout_ns) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -159,17 +164,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint8_t* gb = smem_raw + (sb - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int nqb = (NQ + kBlockM - 1) / kBlockM;
-  const int qb = causal ? (nqb - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
   const int split = static_cast<int>(blockIdx.y);
   const int bh = static_cast<int>(blockIdx.z);
-  const int off = NK - NQ;
-  const int row_hi = min(NQ, (qb + 1) * kBlockM);  // exclusive
-  const int klim_blk = causal ? min(NK, row_hi + off) : NK;
+  // this (batch, head) slice: the whole tensor's sizes, or one sequence of a
+  // packed variable-length batch (the grid covers the longest one)
+  const SeqView sv = PACKED ? seq_view_packed(bh, H, NQ, NK, D, cu_q, cu_k, total_q, total_k)
+                            : seq_view_dense(bh, NQ, NK, D);
+  const int nq = sv.nq, nk = sv.nk;
+  const int nqb = (nq + kBlockM - 1) / kBlockM;
+  const bool active = sv.ok && static_cast<int>(blockIdx.x) < nqb && !(causal && nq > nk);
+  const int qb = causal ? (nqb - 1 - static_cast<int>(blockIdx.x)) : static_cast<int>(blockIdx.x);
+  const int off = nk - nq;
+  const int row_hi = min(nq, (qb + 1) * kBlockM);  // exclusive
+  const int klim_blk = causal ? min(nk, row_hi + off) : nk;
   const int n_tiles = (klim_blk + kBlockN - 1) / kBlockN;
   const int t_begin = SPLIT ? split * tiles_per_split : 0;
   const int t_end = SPLIT ? min(n_tiles, t_begin + tiles_per_split) : n_tiles;
-  int n_iter = max(0, t_end - t_begin);
+  int n_iter = active ? max(0, t_end - t_begin) : 0;
 
   const uint32_t bar0 = sb + L::OFF_BAR;
   const uint32_t q_full = bar0;
@@ -196,6 +207,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     *abort_flag = 0;
     // a failure recorded earlier (this launch or a previous one) skips the work
     *skip_flag = *reinterpret_cast<volatile int*>(dev_status) != 0;
+    // malformed sequence offsets, or a causal sequence with more query rows
+    // than keys (its first rows would see no key): reported, never computed
+    if (!sv.ok || (causal && nq > nk)) atomicCAS(dev_status, 0, kStatusInvalidArg);
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -221,8 +235,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       mbar_arrive_expect_tx(q_full, 2 * L::TILE);
 #pragma unroll
       for (int kb = 0; kb < L::KB; ++kb) {
-        tma_load_3d(sb + L::OFF_Q1 + kb * 16384, &tm_q1, q_full, kb * 64, qb * kBlockM, bh);
-        tma_load_3d(sb + L::OFF_Q2 + kb * 16384, &tm_q2, q_full, kb * 64, qb * kBlockM, bh);
+        tma_load_3d(sb + L::OFF_Q1 + kb * 16384, &tm_q1, q_full, kb * 64, sv.q_row0 + qb * kBlockM,
+                    sv.z);
+        tma_load_3d(sb + L::OFF_Q2 + kb * 16384, &tm_q2, q_full, kb * 64, sv.q_row0 + qb * kBlockM,
+                    sv.z);
       }
       int it = 0;
       for (; it < n_iter; ++it) {
@@ -230,12 +246,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const uint32_t ph = (it / L::STAGES) & 1;
         if (!wait_bounded(kv_empty(s), ph ^ 1, wc)) break;
         mbar_arrive_expect_tx(kv_full(s), 2 * L::TILE);
-        const int krow = (t_begin + it) * kBlockN;
+        const int krow = sv.k_row0 + (t_begin + it) * kBlockN;
         const uint32_t dst = sb + L::OFF_K + s * 2 * L::TILE;
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb) {
-          tma_load_3d(dst + kb * 16384, &tm_k1, kv_full(s), kb * 64, krow, bh);
-          tma_load_3d(dst + L::TILE + kb * 16384, &tm_k2, kv_full(s), kb * 64, krow, bh);
+          tma_load_3d(dst + kb * 16384, &tm_k1, kv_full(s), kb * 64, krow, sv.z);
+          tma_load_3d(dst + L::TILE + kb * 16384, &tm_k2, kv_full(s), kb * 64, krow, sv.z);
         }
       }
       // Let every copy this thread issued land before the CTA can exit.
@@ -282,7 +298,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int r = quarter * 32 + lane;
     const int qrow = qb * kBlockM + r;
     const float c = scale * kLog2e;
-    const int lim = causal ? min(NK, qrow + 1 + off) : NK;
+    const int lim = causal ? min(nk, qrow + 1 + off) : nk;  // keys < lim visible
     RowState st{-INFINITY, 0.f, -INFINITY, 0.f, 0.f};
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * 32;
     for (int it = 0; it < n_iter; ++it) {
@@ -323,10 +339,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                              x[3 * kBlockM + r], x[4 * kBlockM + r]};
         merge_state(st, other);
       }
-      if (qrow < NQ) {
-        const size_t o = static_cast<size_t>(bh) * NQ + qrow;
+      if (active && qrow < nq) {
+        const size_t o = static_cast<size_t>(sv.v_off + static_cast<long long>(qrow) * sv.v_stride);
         if (SPLIT) {
-          const size_t plane = static_cast<size_t>(BH) * NQ;
           const size_t base = static_cast<size_t>(split) * plane + o;
           const size_t fstride = static_cast<size_t>(splits) * plane;
           part[0 * fstride + base] = st.r1;
@@ -376,17 +391,18 @@ __global__ void streamkl_fwd_combine_kernel(const float* __restrict__ part, int 
   lse2_out[i] = l2;
 }
 
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool PACKED>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  auto kern = streamkl_fwd_kernel<D, SPLIT>;
+  auto kern = streamkl_fwd_kernel<D, SPLIT, PACKED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int nqb = (a.NQ + kBlockM - 1) / kBlockM;
   dim3 grid(nqb, SPLIT ? a.splits : 1, a.BH);
   kern<<<grid, kFwdThreads, L::ALLOC, stream>>>(*a.tm_q1, *a.tm_k1, *a.tm_q2, *a.tm_k2, a.NQ, a.NK,
                                                 a.causal, a.scale, a.kl, a.lse1, a.lse2, a.part,
-                                                a.splits, a.tiles_per_split, a.BH, a.dev_status,
+                                                a.splits, a.tiles_per_split, a.plane, a.cu_q, a.cu_k,
+                                                a.H, a.total_q, a.total_k, a.dev_status,
                                                 a.timeout_ns);
   return cudaGetLastError();
 }
@@ -399,12 +415,15 @@ size_t fwd_smem_bytes(int d) {
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
   const bool split = a.splits > 1;
-  if (a.d == 128) return split ? launch_fwd_t<128, true>(a, stream) : launch_fwd_t<128, false>(a, stream);
-  return split ? launch_fwd_t<64, true>(a, stream) : launch_fwd_t<64, false>(a, stream);
+  if (a.cu_q != nullptr)  // packed batches never split
+    return a.d == 128 ? launch_fwd_t<128, false, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);
+  if (a.d == 128)
+    return split ? launch_fwd_t<128, true, false>(a, stream) : launch_fwd_t<128, false, false>(a, stream);
+  return split ? launch_fwd_t<64, true, false>(a, stream) : launch_fwd_t<64, false, false>(a, stream);
 }
 
 cudaError_t launch_fwd_combine(const FwdArgs& a, cudaStream_t stream) {
-  const long long plane = static_cast<long long>(a.BH) * a.NQ;
+  const long long plane = a.plane;
   const int threads = 256;
   const long long blocks = (plane + threads - 1) / threads;
   streamkl_fwd_combine_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(

@@ -10,12 +10,73 @@ namespace skl {
 constexpr int kBlockM = 128;  // query rows per tile
 constexpr int kBlockN = 128;  // keys per tile
 
+// Where one (batch, head) slice of the inputs lives.
+//   dense  [B, H, N, d]:     rows of a head are contiguous (d apart)
+//   packed [total, H, d]:    variable-length batch, sequence b owning rows
+//                            cu[b] .. cu[b+1]; rows of one head are H d apart
+// TMA maps see the dense tensors as {d, N, B H} and the packed ones as
+// {d, total, H}; per-row fp32 vectors (KL, LSE, g) are [B, H, N_Q] or
+// [total_q, H] accordingly.
+struct SeqView {
+  int nq, nk;               // this slice's query and key rows
+  int q_row0, k_row0;       // TMA row coordinate of its row 0
+  int z;                    // TMA third coordinate
+  long long v_off;          // per-row vectors: element of query row 0
+  int v_stride;             // ... and between consecutive query rows
+  long long q_off, k_off;   // bf16 tensors: element (row 0, column 0)
+  long long row_stride;     // elements between consecutive rows
+  bool ok;                  // offsets well formed (packed batches only can fail)
+};
+
+// Dense [B, H, N, d] slice bh (sizes NQ, NK).
+__device__ __forceinline__ SeqView seq_view_dense(int bh, int NQ, int NK, int d) {
+  SeqView v;
+  v.nq = NQ;
+  v.nk = NK;
+  v.q_row0 = v.k_row0 = 0;
+  v.z = bh;
+  v.v_off = static_cast<long long>(bh) * NQ;
+  v.v_stride = 1;
+  v.q_off = static_cast<long long>(bh) * NQ * d;
+  v.k_off = static_cast<long long>(bh) * NK * d;
+  v.row_stride = d;
+  v.ok = true;
+  return v;
+}
+
+// Packed [total, H, d] slice bh = b H + h: sequence b's offsets from cu_q,
+// cu_k (device); max_q, max_k are the lengths the grid was sized for.
+__device__ __forceinline__ SeqView seq_view_packed(int bh, int H, int max_q, int max_k, int d,
+                                                   const int* cu_q, const int* cu_k, int total_q,
+                                                   int total_k) {
+  SeqView v;
+  const int b = bh / H, h = bh - b * H;
+  const int q0 = cu_q[b], q1 = cu_q[b + 1], k0 = cu_k[b], k1 = cu_k[b + 1];
+  v.nq = q1 - q0;
+  v.nk = k1 - k0;
+  v.q_row0 = q0;
+  v.k_row0 = k0;
+  v.z = h;
+  v.v_off = static_cast<long long>(q0) * H + h;
+  v.v_stride = H;
+  v.q_off = (static_cast<long long>(q0) * H + h) * d;
+  v.k_off = (static_cast<long long>(k0) * H + h) * d;
+  v.row_stride = static_cast<long long>(H) * d;
+  v.ok = q0 >= 0 && k0 >= 0 && v.nq >= 0 && v.nk >= 0 && v.nq <= max_q && v.nk <= max_k &&
+         q1 <= total_q && k1 <= total_k;
+  return v;
+}
+
 struct FwdArgs {
   const CUtensorMap* tm_q1;
   const CUtensorMap* tm_k1;
   const CUtensorMap* tm_q2;
   const CUtensorMap* tm_k2;
   int BH, NQ, NK, d, causal;
+  const int* cu_q = nullptr;  // packed variable-length batch (device offsets), else null
+  const int* cu_k = nullptr;
+  int H = 1, total_q = 0, total_k = 0;
+  long long plane = 0;        // per-row vector entries (B H N_Q, or total_q H)
   float scale;
   float* kl;
   float* lse1;
@@ -52,6 +113,9 @@ struct BwdSepArgs {
   const CUtensorMap* tm_q2;
   const CUtensorMap* tm_k2;
   int BH, NQ, NK, d, causal;
+  const int* cu_q = nullptr;  // packed variable-length batch (device offsets), else null
+  const int* cu_k = nullptr;
+  int H = 1, total_q = 0, total_k = 0;
   int grad1, grad2;  // gradient sets wanted: dQ1/dK1 (configuration 2), dQ2/dK2 (configuration 1)
   float scale;
   const float* kl;

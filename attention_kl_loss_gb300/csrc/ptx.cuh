@@ -14,7 +14,8 @@
 
 namespace skl {
 
-constexpr int kStatusTimeout = 4;  // == STREAMKL_ERR_TIMEOUT
+constexpr int kStatusInvalidArg = 1;  // == STREAMKL_ERR_INVALID_ARG
+constexpr int kStatusTimeout = 4;     // == STREAMKL_ERR_TIMEOUT
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

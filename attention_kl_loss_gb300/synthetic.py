@@ -107,3 +107,31 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu"):
     g = torch.full((w.B, w.H, w.NQ), 1.0 / (w.B * w.H * w.NQ), device=device,
                    dtype=torch.float32)
     return q1, k1, q2, k2, g
+
+
+def make_packed_inputs(lens_q, lens_k, H: int, d: int, seed: int = 0, noise: float = 0.3,
+                       device="cpu"):
+    """A packed variable-length batch: sequence b has lens_q[b] query rows and
+    lens_k[b] key rows. Returns (q1, k1, q2, k2, g, cu_q, cu_k): bf16
+    [total, H, d] x4 (teacher ~ N(0,1), student = teacher + noise N(0,1)),
+    fp32 g [total_q, H] = 1 / (H total_q), int32 offsets [B + 1]."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    tq, tk = int(sum(lens_q)), int(sum(lens_k))
+
+    def draw(rows):
+        return torch.randn((rows, H, d), generator=gen, device=device, dtype=torch.float32)
+
+    q1f, k1f = draw(tq), draw(tk)
+    q2f = draw(tq).mul_(noise).add_(q1f)
+    k2f = draw(tk).mul_(noise).add_(k1f)
+    q1, k1, q2, k2 = (t.to(torch.bfloat16) for t in (q1f, k1f, q2f, k2f))
+    g = torch.full((tq, H), 1.0 / (H * max(tq, 1)), device=device, dtype=torch.float32)
+
+    def offsets(lens):
+        cu = [0]
+        for n in lens:
+            cu.append(cu[-1] + int(n))
+        return torch.tensor(cu, dtype=torch.int32, device=device)
+
+    return q1, k1, q2, k2, g, offsets(lens_q), offsets(lens_k)

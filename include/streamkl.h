@@ -177,6 +177,47 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
                              void* workspace, size_t ws_bytes, int* dev_status, void* stream);
 
 /*
+ * Variable-length batches (packed, token-major). The same forward as
+ * streamkl_fwd for B independent sequences of different lengths, each with
+ * H heads (gist.science technical summary, section 1: the streaming pass is
+ * per (batch, head) row and never needs the other sequences' keys).
+ *   in : q1, q2 bf16 [total_q, H, d]; k1, k2 bf16 [total_k, H, d] (16-byte
+ *        aligned, d contiguous, heads next, then tokens); cu_seqlens_q,
+ *        cu_seqlens_k: DEVICE int32 arrays of B+1 offsets, 0 = cu[0] <= cu[1]
+ *        <= ... <= cu[B] = total: sequence b owns query rows cu_seqlens_q[b]
+ *        .. cu_seqlens_q[b+1] and key rows cu_seqlens_k[b] .. cu_seqlens_k[b+1];
+ *        max_seqlen_q / max_seqlen_k: upper bounds on the per-sequence lengths
+ *        (they size the grid); causal: per sequence, bottom-right aligned.
+ *   out: kl, lse1, lse2 fp32 [total_q, H].
+ * No split-K and no workspace. Host-side errors as for streamkl_fwd; the
+ * offsets live on the device, so the kernels check them and write
+ * STREAMKL_ERR_INVALID_ARG into *dev_status for offsets outside [0, total],
+ * a length above its max_seqlen, or a causal sequence with more query rows
+ * than keys (its rows of that sequence are then left unwritten).
+ */
+streamkl_status streamkl_fwd_varlen(const void* q1, const void* k1, const void* q2, const void* k2,
+                                    const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                                    int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                                    int d, float scale, int causal, float* kl, float* lse1,
+                                    float* lse2, int* dev_status, void* stream);
+
+/*
+ * Backward of L = sum dkl * KL for a packed variable-length batch: inputs
+ * and sequence offsets as for streamkl_fwd_varlen; kl, lse1, lse2, dkl fp32
+ * [total_q, H]; gradients bf16 [total_q, H, d] (dq2, dq1) and [total_k, H, d]
+ * (dk2, dk1), either pair NULL to skip that configuration (at least one
+ * pair). Always the separate dK/dQ kernels; no workspace. Errors as for
+ * streamkl_bwd and streamkl_fwd_varlen.
+ */
+streamkl_status streamkl_bwd_varlen(const void* q1, const void* k1, const void* q2, const void* k2,
+                                    const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                                    int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,
+                                    int d, float scale, int causal, const float* kl,
+                                    const float* lse1, const float* lse2, const float* dkl,
+                                    void* dq2, void* dk2, void* dq1, void* dk1, int* dev_status,
+                                    void* stream);
+
+/*
  * Self-test of the bounded-wait path: launches one tiny kernel that waits on
  * a barrier nothing arrives on, for timeout_us microseconds, then records
  * STREAMKL_ERR_TIMEOUT in *dev_status and returns. No other state is touched.

@@ -166,3 +166,24 @@ def test_pair_counts():
     w4 = synthetic.WORKLOADS["splitk"]
     brute = sum(i + 1 + (131072 - 512) for i in range(512))
     assert w4.live_pairs_per_head() == brute
+
+
+def test_packed_batch_validation(lib):
+    """Host checks of the variable-length entry points (the offsets are device
+    data and are checked by the kernels)."""
+    P = ctypes.c_void_p
+    a, cu = P(0x1000), P(0x2000)
+
+    def fwd(cu_q=cu, cu_k=cu, total_q=300, total_k=400, max_q=200, max_k=250, d=64):
+        return lib.streamkl_fwd_varlen(a, a, a, a, cu_q, cu_k, 2, 4, total_q, total_k, max_q, max_k,
+                                       d, 0.125, 1, a, a, a, a, None)
+
+    assert fwd(cu_q=None) == 1
+    assert b"cu_seqlens" in lib.streamkl_last_error()
+    assert fwd(cu_q=P(0x2002)) == 1  # misaligned offsets
+    assert fwd(max_q=301) == 1  # longer than the packed total
+    assert fwd(total_k=0) == 1
+    assert fwd(d=96) == 2
+    st = lib.streamkl_bwd_varlen(a, a, a, a, cu, cu, 2, 4, 300, 400, 200, 250, 64, 0.125, 1, a, a,
+                                 a, a, None, None, None, None, a, None)
+    assert st == 1 and b"no gradient" in lib.streamkl_last_error()
