@@ -363,6 +363,10 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     // part of a warp); then the T GEMMs of step it+1 may overwrite T
     float a[16], b[16];
     auto load_t = [&](int it) {
+      // dK kernel: the stage's barrier also publishes its constant table; its
+      // phase completed before these T GEMMs were issued, so test it first
+      // and let the round trip overlap the T wait
+      const bool tab = DQ || mbar_test_wait(y_full(it % kStages), (it / kStages) & 1);
       if (!__all_sync(0xffffffffu, wait_bounded(s_full, it & 1, wc))) return false;
       tc_fence_after();
       tmem_ld16(tmem + lane_off + L::COL_T + grp * 16, a);
@@ -371,8 +375,8 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
-      // dK kernel: the stage's barrier also publishes its constant table
-      return DQ || __all_sync(0xffffffffu, wait_bounded(y_full(it % kStages), (it / kStages) & 1, wc));
+      return DQ || __all_sync(0xffffffffu, tab) ||
+             __all_sync(0xffffffffu, wait_bounded(y_full(it % kStages), (it / kStages) & 1, wc));
     };
     // The next step's T is loaded right after this step's dS is computed and
     // before it is stored, so the next T GEMMs can start as early as possible.
@@ -383,6 +387,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         break;
       }
       const int y0 = (y_begin + it) * kStepRows + grp * 16;  // first Y row of this thread's columns
+      // the gradient GEMMs of step it-2 have read this step's dS buffer: nearly
+      // always done by now; test early, block only if not
+      const bool ds_ready = mbar_test_wait(ds_free(it & 1), ((it >> 1) & 1) ^ 1);
       uint32_t d2p[8], d1p[8];
       {
         // visibility of (query, key) over this thread's 16 columns
@@ -445,14 +452,15 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         }
       }
       if (it + 1 < n_iter) good = load_t(it + 1);
-      // the gradient GEMMs of step it-2 have read this dS buffer
-      if (!__all_sync(0xffffffffu, wait_bounded(ds_free(it & 1), ((it >> 1) & 1) ^ 1, wc))) {
+      if (!__all_sync(0xffffffffu, ds_ready) &&
+          !__all_sync(0xffffffffu, wait_bounded(ds_free(it & 1), ((it >> 1) & 1) ^ 1, wc))) {
         ok = false;
         break;
       }
       // this thread's 16 values of row r: 8 packed columns per set at
       // [8 grp, 8 grp + 8) of the set's 32-column slot of buffer it&1
       const uint32_t dsb = tmem + lane_off + L::COL_DS + (it & 1) * 64 + grp * 8;
+      tc_fence_after();  // the stores below follow the MMAs that read this buffer
       if (HAS2) tmem_st8(dsb, d2p);
       if (HAS1) tmem_st8(dsb + (HAS2 ? 32 : 0), d1p);
       tmem_wait_st();
