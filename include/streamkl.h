@@ -77,10 +77,9 @@ size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int caus
  *       its whole sweep; no atomics, no workspace;
  *   1 = one fused kernel per key tile: dK on chip, dQ reduced into an fp32
  *       workspace with global atomics, then converted to bf16.
- * The automatic choice is 0 except for configuration 1 alone (want_grad1 = 0)
- * at d = 128 with 129..512 query rows and at least 128 keys per query row,
- * where the fused kernel measured faster on GB300. Returns -1 on invalid
- * sizes.
+ * The automatic choice is 0: on GB300 the separate kernels measured at least
+ * as fast on every shape tried; 1 only when forced (below). Returns -1 on
+ * invalid sizes.
  */
 int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int want_grad1);
 

@@ -83,17 +83,12 @@ def test_workspace_sizes(lib):
 
 def test_automatic_backward_choice(lib):
     lib.streamkl_set_bwd_algorithm(-1)
-    # separate kernels by default
-    assert lib.streamkl_bwd_algorithm(1, 32, 65536, 65536, 128, 1, 1) == 0
-    assert lib.streamkl_bwd_algorithm(4, 32, 64, 65536, 128, 1, 0) == 0
-    assert lib.streamkl_bwd_algorithm(4, 32, 1024, 131072, 128, 1, 0) == 0
-    # fused: configuration 1 alone, short query range over many keys, d = 128
-    assert lib.streamkl_bwd_algorithm(4, 32, 512, 131072, 128, 1, 0) == 1
-    assert lib.streamkl_bwd_algorithm(4, 32, 256, 65536, 128, 1, 0) == 1
-    assert lib.streamkl_bwd_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 4 * 32 * 512 * 128 * 4
-    # ... but not with both gradient sets or at d = 64
-    assert lib.streamkl_bwd_algorithm(4, 32, 512, 131072, 128, 1, 1) == 0
-    assert lib.streamkl_bwd_algorithm(4, 32, 512, 131072, 64, 1, 0) == 0
+    # separate kernels on every shape unless forced
+    for args in [(1, 32, 65536, 65536, 128, 1, 1), (4, 32, 64, 65536, 128, 1, 0),
+                 (4, 32, 512, 131072, 128, 1, 0), (4, 32, 256, 65536, 128, 1, 0),
+                 (4, 32, 512, 131072, 64, 1, 0)]:
+        assert lib.streamkl_bwd_algorithm(*args) == 0, args
+    assert lib.streamkl_bwd_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 0
 
 
 def test_forced_split_workspace_rounding(lib):
