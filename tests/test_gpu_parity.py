@@ -139,6 +139,28 @@ def test_ragged_shapes_one_gradient_set(NQ, NK, d, causal, algo):
     full_check(w, seed=NQ * 3 + NK, grad1=False, algo=algo)
 
 
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("NQ,NK,d,causal", [(300, 300, 128, True), (200, 257, 64, False)])
+def test_upstream_gradient_of_either_sign(NQ, NK, d, causal, algo):
+    """g per row drawn from N(0,1) (negative, positive, one row exactly 0):
+    the gradient is linear in g row by row."""
+    w = synthetic.custom(f"gsign_{NQ}x{NK}d{d}", B=1, H=4, NQ=NQ, NK=NK, d=d, causal=causal,
+                         noise=0.4, grad1=True)
+    dev = torch.device("cuda")
+    q1, k1, q2, k2, _ = synthetic.make_inputs(w, 21, dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(22)
+    g = torch.randn((w.B, w.H, w.NQ), generator=gen, device=dev, dtype=torch.float32)
+    g[0, 1, 7] = 0.0
+    ins, outs, grads = run(w, inputs=(q1, k1, q2, k2, g), algo=algo)
+    for hh in range(w.H):
+        h = [host(t[0, hh]) for t in ins[:4]]
+        og = orc.head_backward(*h, w.scale, w.causal, g[0, hh].cpu().numpy().astype(np.float64),
+                               True)
+        for i, name in enumerate(["dq2", "dk2", "dq1", "dk1"]):
+            assert_grad(host(grads[i][0, hh]), og[i], name)
+
+
 @pytest.mark.parametrize("NQ,NK,d,causal", [(256, 256, 64, False), (200, 333, 128, True),
                                              (130, 131, 64, True)])
 def test_configuration2_only(NQ, NK, d, causal):
