@@ -17,9 +17,11 @@ from .binding import (  # noqa: F401
     selftest_wait_timeout,
     set_bwd_algorithm,
     streamkl_bwd,
+    streamkl_bwd_reverse,
     streamkl_bwd_varlen,
     streamkl_bwd_workspace_size,
     streamkl_fwd,
+    streamkl_fwd_reverse,
     streamkl_fwd_noalloc,
     streamkl_fwd_varlen,
     streamkl_fwd_workspace_size,

@@ -40,6 +40,10 @@ _SIGNATURES = {
                           _P, _P]),
     "streamkl_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P, _P,
                           _P, _P, _P, _Z, _P, _P]),
+    "streamkl_fwd_reverse": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P,
+                                  _P, _Z, _P, _P]),
+    "streamkl_bwd_reverse": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P,
+                                  _P, _P, _P, _P, _Z, _P, _P]),
     "streamkl_selftest_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
     "streamkl_bwd_algorithm": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "streamkl_set_bwd_algorithm": (_I, [_I]),
@@ -157,9 +161,8 @@ def _workspace(nbytes: int, device, workspace):
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
-def streamkl_fwd(q1, k1, q2, k2, scale: Optional[float] = None, causal: bool = False,
-                 num_splits: int = 0, out=None, workspace=None, dev_status=None, stream=None):
-    """Per-row KL(P1||P2), lse1, lse2 (fp32 [B, H, N_Q]) via the CUDA library."""
+def _fwd_call(entry, q1, k1, q2, k2, scale, causal, num_splits, out, workspace, dev_status,
+              stream):
     lib = load()
     B, H, NQ, NK, d = _dims(q1, k1, q2, k2)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
@@ -170,12 +173,27 @@ def streamkl_fwd(q1, k1, q2, k2, scale: Optional[float] = None, causal: bool = F
     need = streamkl_fwd_workspace_size(B, H, NQ, NK, d, causal, num_splits)
     ws = _workspace(need, dev, workspace)
     status = dev_status if dev_status is not None else new_status(dev)
-    st = lib.streamkl_fwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), B, H, NQ, NK, d, scale,
-                          int(causal), int(num_splits), _ptr(kl), _ptr(lse1), _ptr(lse2),
-                          _ptr(ws), need if ws is not None else 0, _ptr(status),
-                          _stream_handle(stream))
-    _check(st, "streamkl_fwd")
+    st = getattr(lib, entry)(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), B, H, NQ, NK, d, scale,
+                             int(causal), int(num_splits), _ptr(kl), _ptr(lse1), _ptr(lse2),
+                             _ptr(ws), need if ws is not None else 0, _ptr(status),
+                             _stream_handle(stream))
+    _check(st, entry)
     return kl, lse1, lse2
+
+
+def streamkl_fwd(q1, k1, q2, k2, scale: Optional[float] = None, causal: bool = False,
+                 num_splits: int = 0, out=None, workspace=None, dev_status=None, stream=None):
+    """Per-row KL(P1||P2), lse1, lse2 (fp32 [B, H, N_Q]) via the CUDA library."""
+    return _fwd_call("streamkl_fwd", q1, k1, q2, k2, scale, causal, num_splits, out, workspace,
+                     dev_status, stream)
+
+
+def streamkl_fwd_reverse(q1, k1, q2, k2, scale: Optional[float] = None, causal: bool = False,
+                         num_splits: int = 0, out=None, workspace=None, dev_status=None,
+                         stream=None):
+    """Per-row KL(P2||P1) (the reverse direction), lse1, lse2 (fp32 [B, H, N_Q])."""
+    return _fwd_call("streamkl_fwd_reverse", q1, k1, q2, k2, scale, causal, num_splits, out,
+                     workspace, dev_status, stream)
 
 
 def streamkl_fwd_noalloc(q1, k1, q2, k2, out, scale: Optional[float] = None,
@@ -198,12 +216,8 @@ def streamkl_fwd_noalloc(q1, k1, q2, k2, out, scale: Optional[float] = None,
     return kl, lse1, lse2
 
 
-def streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = None,
-                 causal: bool = False, grad1: bool = False, out=None, workspace=None,
-                 dev_status=None, stream=None, grad2: bool = True):
-    """Gradients of sum(dkl * KL): (dq2, dk2, dq1, dk1), bf16. dq2/dk2
-    (configuration 1, P1 fixed) unless ``grad2`` is False; dq1/dk1
-    (configuration 2, P2 fixed) only with ``grad1``; skipped ones are None."""
+def _bwd_call(entry, q1, k1, q2, k2, kl, lse1, lse2, dkl, scale, causal, grad1, grad2, out,
+              workspace, dev_status, stream, ws_sets):
     if not (grad1 or grad2):
         raise ValueError("no gradient requested (grad1 and grad2 both False)")
     lib = load()
@@ -220,15 +234,42 @@ def streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = N
         dk1 = torch.empty_like(k1) if grad1 else None
     else:
         dq2, dk2, dq1, dk1 = out
-    need = streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal, grad1)
+    need = ws_sets(B, H, NQ, NK, d)
     ws = _workspace(need, dev, workspace)
     status = dev_status if dev_status is not None else new_status(dev)
-    st = lib.streamkl_bwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), B, H, NQ, NK, d, scale,
-                          int(causal), _ptr(kl), _ptr(lse1), _ptr(lse2), _ptr(dkl), _ptr(dq2),
-                          _ptr(dk2), _ptr(dq1), _ptr(dk1), _ptr(ws), need, _ptr(status),
-                          _stream_handle(stream))
-    _check(st, "streamkl_bwd")
+    st = getattr(lib, entry)(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), B, H, NQ, NK, d, scale,
+                             int(causal), _ptr(kl), _ptr(lse1), _ptr(lse2), _ptr(dkl), _ptr(dq2),
+                             _ptr(dk2), _ptr(dq1), _ptr(dk1), _ptr(ws), need, _ptr(status),
+                             _stream_handle(stream))
+    _check(st, entry)
     return dq2, dk2, dq1, dk1
+
+
+def streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = None,
+                 causal: bool = False, grad1: bool = False, out=None, workspace=None,
+                 dev_status=None, stream=None, grad2: bool = True):
+    """Gradients of sum(dkl * KL): (dq2, dk2, dq1, dk1), bf16. dq2/dk2
+    (configuration 1, P1 fixed) unless ``grad2`` is False; dq1/dk1
+    (configuration 2, P2 fixed) only with ``grad1``; skipped ones are None."""
+    return _bwd_call("streamkl_bwd", q1, k1, q2, k2, kl, lse1, lse2, dkl, scale, causal, grad1,
+                     grad2, out, workspace, dev_status, stream,
+                     lambda B, H, NQ, NK, d: streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal,
+                                                                         grad1))
+
+
+def streamkl_bwd_reverse(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = None,
+                         causal: bool = False, grad1: bool = False, out=None, workspace=None,
+                         dev_status=None, stream=None, grad2: bool = True):
+    """Gradients of sum(dkl * KL(P2||P1)), with kl, lse1, lse2 from
+    streamkl_fwd_reverse: (dq2, dk2, dq1, dk1), bf16. dq2/dk2 (the student's,
+    P1 fixed) unless ``grad2`` is False; dq1/dk1 (the teacher's, P2 fixed)
+    only with ``grad1``; skipped ones are None."""
+    # the exchanged call needs a workspace only with the teacher's gradients
+    # (its configuration 1), sized for the student's set as well when present
+    return _bwd_call("streamkl_bwd_reverse", q1, k1, q2, k2, kl, lse1, lse2, dkl, scale, causal,
+                     grad1, grad2, out, workspace, dev_status, stream,
+                     lambda B, H, NQ, NK, d: (streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal,
+                                                                          grad2) if grad1 else 0))
 
 
 def _packed_dims(q1, k1, q2, k2, cu_seqlens_q, cu_seqlens_k):

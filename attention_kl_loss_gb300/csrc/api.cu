@@ -527,6 +527,36 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   return STREAMKL_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Reverse direction KL(P2 || P1): the teacher-first computation with the two
+// distributions exchanged. Only the argument slots move.
+streamkl_status streamkl_fwd_reverse(const void* q1, const void* k1, const void* q2, const void* k2,
+                                     int B, int H, int NQ, int NK, int d, float scale, int causal,
+                                     int num_splits, float* kl, float* lse1, float* lse2,
+                                     void* workspace, size_t ws_bytes, int* dev_status,
+                                     void* stream) {
+  return streamkl_fwd(q2, k2, q1, k1, B, H, NQ, NK, d, scale, causal, num_splits, kl, lse2, lse1,
+                      workspace, ws_bytes, dev_status, stream);
+}
+
+streamkl_status streamkl_bwd_reverse(const void* q1, const void* k1, const void* q2, const void* k2,
+                                     int B, int H, int NQ, int NK, int d, float scale, int causal,
+                                     const float* kl, const float* lse1, const float* lse2,
+                                     const float* dkl, void* dq2, void* dk2, void* dq1, void* dk1,
+                                     void* workspace, size_t ws_bytes, int* dev_status,
+                                     void* stream) {
+  g_err[0] = '\0';
+  if ((dq2 == nullptr) != (dk2 == nullptr))
+    return fail(STREAMKL_ERR_INVALID_ARG, "dq2 and dk2 must be both NULL or both non-NULL");
+  if ((dq1 == nullptr) != (dk1 == nullptr))
+    return fail(STREAMKL_ERR_INVALID_ARG, "dq1 and dk1 must be both NULL or both non-NULL");
+  // In the exchanged call the student is the first distribution: its
+  // gradients are that call's configuration-2 outputs (dq1/dk1 slots), the
+  // teacher's its configuration-1 outputs (dq2/dk2 slots).
+  return streamkl_bwd(q2, k2, q1, k1, B, H, NQ, NK, d, scale, causal, kl, lse2, lse1, dkl, dq1, dk1,
+                      dq2, dk2, workspace, ws_bytes, dev_status, stream);
+}
+
 streamkl_status streamkl_fwd_varlen(const void* q1, const void* k1, const void* q2, const void* k2,
                                     const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
                                     int total_q, int total_k, int max_seqlen_q, int max_seqlen_k,

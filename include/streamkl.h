@@ -176,6 +176,36 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
                              void* workspace, size_t ws_bytes, int* dev_status, void* stream);
 
 /*
+ * Reverse direction, KL(P2 || P1) per row. The pages define the
+ * teacher-first direction KL(P1 || P2) only (gist.science technical summary,
+ * "Declaracion del Problema"); the reverse one is the same computation with
+ * the two distributions exchanged, so these two calls run the kernels above
+ * with the argument slots swapped and add nothing else.
+ *   streamkl_fwd_reverse: arguments as for streamkl_fwd; out: kl[b,h,i] =
+ *        KL(P2 || P1) of row i, lse1 / lse2 the log-partition of S1 / S2
+ *        exactly as from streamkl_fwd.
+ *   streamkl_bwd_reverse: gradients of L = sum dkl * KL(P2 || P1), with kl,
+ *        lse1, lse2 from streamkl_fwd_reverse. dq2, dk2 get the student's
+ *        gradients (P1 fixed), dq1, dk1 the teacher's (P2 fixed); either pair
+ *        may be NULL to skip it (at least one pair). With the teacher pair
+ *        NULL no workspace is needed; ws_bytes >= streamkl_bwd_workspace_size(
+ *        ..., want_grad1 = 1) always suffices.
+ * Errors as for streamkl_fwd / streamkl_bwd; a message about a tensor names
+ * it by its slot in the exchanged call (q1 for the q2 given here, and so on).
+ */
+streamkl_status streamkl_fwd_reverse(const void* q1, const void* k1, const void* q2,
+                                     const void* k2, int B, int H, int NQ, int NK, int d,
+                                     float scale, int causal, int num_splits, float* kl,
+                                     float* lse1, float* lse2, void* workspace, size_t ws_bytes,
+                                     int* dev_status, void* stream);
+streamkl_status streamkl_bwd_reverse(const void* q1, const void* k1, const void* q2,
+                                     const void* k2, int B, int H, int NQ, int NK, int d,
+                                     float scale, int causal, const float* kl, const float* lse1,
+                                     const float* lse2, const float* dkl, void* dq2, void* dk2,
+                                     void* dq1, void* dk1, void* workspace, size_t ws_bytes,
+                                     int* dev_status, void* stream);
+
+/*
  * Variable-length batches (packed, token-major). The same forward as
  * streamkl_fwd for B independent sequences of different lengths, each with
  * H heads (gist.science technical summary, section 1: the streaming pass is

@@ -149,6 +149,45 @@ def test_backward_validation(lib):
         lib.streamkl_set_bwd_algorithm(-1)
 
 
+def test_reverse_direction_validation(lib):
+    """The reverse entry points check their own gradient pairs by their own
+    names and otherwise fail exactly like the exchanged forward/backward call."""
+    P = ctypes.c_void_p
+    a = P(0x1000)
+    f = lambda v: P(v) if v else None
+
+    def fwd_rev(q1=0x1000, q2=0x1000, d=64, NQ=8, NK=8, causal=0):
+        return lib.streamkl_fwd_reverse(f(q1), a, f(q2), a, 1, 1, NQ, NK, d, 0.125, causal, 0, a,
+                                        a, a, None, 0, a, None)
+
+    assert fwd_rev(q2=0) == 1
+    assert b"q1" in lib.streamkl_last_error()  # named by its slot in the exchanged call
+    assert fwd_rev(q1=0x1001) == 1  # misaligned
+    assert fwd_rev(d=96) == 2
+    assert fwd_rev(NQ=16, NK=8, causal=1) == 1
+
+    def bwd_rev(dq2, dk2, dq1, dk1, status=None, ws=None, ws_bytes=0):
+        return lib.streamkl_bwd_reverse(a, a, a, a, 1, 1, 8, 8, 64, 0.125, 0, a, a, a, a, f(dq2),
+                                        f(dk2), f(dq1), f(dk1), f(ws), ws_bytes, f(status), None)
+
+    assert bwd_rev(0x1000, 0, 0, 0) == 1
+    assert b"dq2 and dk2" in lib.streamkl_last_error()
+    assert bwd_rev(0, 0, 0, 0x1000) == 1
+    assert b"dq1 and dk1" in lib.streamkl_last_error()
+    assert bwd_rev(0, 0, 0, 0) == 1
+    assert b"no gradient" in lib.streamkl_last_error()
+    # the student's gradients alone pass every check but the missing status word
+    assert bwd_rev(0x1000, 0x1000, 0, 0) == 1
+    assert b"dev_status" in lib.streamkl_last_error()
+    try:
+        lib.streamkl_set_bwd_algorithm(1)
+        # with the teacher's gradients the fused algorithm needs its workspace
+        assert bwd_rev(0x1000, 0x1000, 0x1000, 0x1000, status=0x3000) == 1
+        assert b"workspace" in lib.streamkl_last_error()
+    finally:
+        lib.streamkl_set_bwd_algorithm(-1)
+
+
 def test_selftest_validation(lib):
     assert lib.streamkl_selftest_wait_timeout(None, 100, None) == 1
     assert lib.streamkl_selftest_wait_timeout(ctypes.c_void_p(0x1000), 0, None) == 1

@@ -190,6 +190,47 @@ def test_configuration2_only(NQ, NK, d, causal):
 
 
 @pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("NQ,NK,d,causal", [(256, 256, 64, False), (200, 333, 128, True)])
+def test_reverse_direction(NQ, NK, d, causal, algo):
+    """KL(P2 || P1) and its gradients through the reverse entry points, against
+    the oracle's definition with the two distributions given in that order:
+    the student's gradients (P1 fixed) alone and with the teacher's."""
+    w = synthetic.custom(f"rev_{NQ}x{NK}d{d}", B=2, H=2, NQ=NQ, NK=NK, d=d, causal=causal,
+                         noise=0.5, grad1=True)
+    dev = torch.device("cuda")
+    ins = synthetic.make_inputs(w, 11, dev)
+    q1, k1, q2, k2, g = ins
+    status = binding.new_status(dev)
+    kl, lse1, lse2 = binding.streamkl_fwd_reverse(q1, k1, q2, k2, w.scale, w.causal,
+                                                  dev_status=status)
+    student = binding.streamkl_bwd_reverse(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                           dev_status=status)
+    binding.set_bwd_algorithm(algo)
+    try:
+        both = binding.streamkl_bwd_reverse(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                            grad1=True, dev_status=status)
+    finally:
+        binding.set_bwd_algorithm(None)
+    binding.raise_on_device_status(status, "reverse direction")
+    assert student[2] is None and student[3] is None
+    for b in range(w.B):
+        for hh in range(w.H):
+            h1q, h1k, h2q, h2k = (host(t[b, hh]) for t in ins[:4])
+            rkl, rl2, rl1 = orc.head_forward(h2q, h2k, h1q, h1k, w.scale, w.causal)
+            assert_kl(host(kl[b, hh]), rkl)
+            assert rel_l2(host(lse1[b, hh]), rl1) <= LSE_REL
+            assert rel_l2(host(lse2[b, hh]), rl2) <= LSE_REL
+            gr = g[b, hh].cpu().numpy().astype(np.float64)
+            # oracle order (second, first): teacher dq, teacher dk, student dq, student dk
+            t_dq, t_dk, s_dq, s_dk = orc.head_backward(h2q, h2k, h1q, h1k, w.scale, w.causal, gr,
+                                                       True)
+            for got, ref, name in ((student[0], s_dq, "student dq2"), (student[1], s_dk, "student dk2"),
+                                   (both[0], s_dq, "dq2"), (both[1], s_dk, "dk2"),
+                                   (both[2], t_dq, "teacher dq1"), (both[3], t_dk, "teacher dk1")):
+                assert_grad(host(got[b, hh]), ref, name)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("d", [64, 128])
 def test_peaked_teacher_independent_student(d, algo):
     w = synthetic.custom("peaked", B=1, H=2, NQ=384, NK=640, d=d, causal=False, teacher_std=3.0,
