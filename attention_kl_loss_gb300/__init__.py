@@ -10,12 +10,14 @@ from .binding import (  # noqa: F401
     BWD_SEPARATE,
     StreamKLError,
     bwd_algorithm,
+    bwd_dq_splits,
     choose_splits,
     load,
     new_status,
     raise_on_device_status,
     selftest_wait_timeout,
     set_bwd_algorithm,
+    set_bwd_dq_splits,
     streamkl_bwd,
     streamkl_bwd_reverse,
     streamkl_bwd_varlen,

@@ -47,6 +47,8 @@ _SIGNATURES = {
     "streamkl_selftest_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
     "streamkl_bwd_algorithm": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "streamkl_set_bwd_algorithm": (_I, [_I]),
+    "streamkl_bwd_dq_splits": (_I, [_I, _I, _I, _I, _I, _I, _I]),
+    "streamkl_set_bwd_dq_splits": (_I, [_I]),
     "streamkl_fwd_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P,
                                   _P, _P]),
     "streamkl_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
@@ -139,6 +141,17 @@ def bwd_algorithm(B, H, NQ, NK, d, causal, want_grad1=False) -> int:
     return int(load().streamkl_bwd_algorithm(B, H, NQ, NK, d, int(causal), int(want_grad1)))
 
 
+def bwd_dq_splits(B, H, NQ, NK, d, causal, want_grad1=False) -> int:
+    """Key splits of the separate backward's dQ kernel for these sizes."""
+    return int(load().streamkl_bwd_dq_splits(B, H, NQ, NK, d, int(causal), int(want_grad1)))
+
+
+def set_bwd_dq_splits(splits: Optional[int]) -> None:
+    """Force the dQ kernel's key splits (None or 0: automatic)."""
+    if load().streamkl_set_bwd_dq_splits(0 if splits is None else int(splits)) != 0:
+        raise ValueError(f"invalid dQ split count {splits!r}")
+
+
 def set_bwd_algorithm(algo: Optional[int]) -> None:
     """Force the backward algorithm process-wide (None = automatic)."""
     v = -1 if algo is None else int(algo)
@@ -217,7 +230,7 @@ def streamkl_fwd_noalloc(q1, k1, q2, k2, out, scale: Optional[float] = None,
 
 
 def _bwd_call(entry, q1, k1, q2, k2, kl, lse1, lse2, dkl, scale, causal, grad1, grad2, out,
-              workspace, dev_status, stream, ws_sets):
+              workspace, dev_status, stream):
     if not (grad1 or grad2):
         raise ValueError("no gradient requested (grad1 and grad2 both False)")
     lib = load()
@@ -234,7 +247,9 @@ def _bwd_call(entry, q1, k1, q2, k2, kl, lse1, lse2, dkl, scale, causal, grad1, 
         dk1 = torch.empty_like(k1) if grad1 else None
     else:
         dq2, dk2, dq1, dk1 = out
-    need = ws_sets(B, H, NQ, NK, d)
+    # sized for the sets requested (want_grad1 = both), which covers either
+    # direction: the fused kernel's accumulators or the dQ split's partials
+    need = streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal, grad1 and grad2)
     ws = _workspace(need, dev, workspace)
     status = dev_status if dev_status is not None else new_status(dev)
     st = getattr(lib, entry)(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), B, H, NQ, NK, d, scale,
@@ -252,9 +267,7 @@ def streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = N
     (configuration 1, P1 fixed) unless ``grad2`` is False; dq1/dk1
     (configuration 2, P2 fixed) only with ``grad1``; skipped ones are None."""
     return _bwd_call("streamkl_bwd", q1, k1, q2, k2, kl, lse1, lse2, dkl, scale, causal, grad1,
-                     grad2, out, workspace, dev_status, stream,
-                     lambda B, H, NQ, NK, d: streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal,
-                                                                         grad1))
+                     grad2, out, workspace, dev_status, stream)
 
 
 def streamkl_bwd_reverse(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[float] = None,
@@ -264,12 +277,8 @@ def streamkl_bwd_reverse(q1, k1, q2, k2, kl, lse1, lse2, dkl, scale: Optional[fl
     streamkl_fwd_reverse: (dq2, dk2, dq1, dk1), bf16. dq2/dk2 (the student's,
     P1 fixed) unless ``grad2`` is False; dq1/dk1 (the teacher's, P2 fixed)
     only with ``grad1``; skipped ones are None."""
-    # the exchanged call needs a workspace only with the teacher's gradients
-    # (its configuration 1), sized for the student's set as well when present
     return _bwd_call("streamkl_bwd_reverse", q1, k1, q2, k2, kl, lse1, lse2, dkl, scale, causal,
-                     grad1, grad2, out, workspace, dev_status, stream,
-                     lambda B, H, NQ, NK, d: (streamkl_bwd_workspace_size(B, H, NQ, NK, d, causal,
-                                                                          grad2) if grad1 else 0))
+                     grad1, grad2, out, workspace, dev_status, stream)
 
 
 def _packed_dims(q1, k1, q2, k2, cu_seqlens_q, cu_seqlens_k):

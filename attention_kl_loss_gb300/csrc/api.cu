@@ -184,6 +184,66 @@ size_t bwd_ws(int B, int H, int NQ, int NK, int d, int grad1) {
   return grad1 ? 2 * one : one;
 }
 
+// Key split of the separate backward's dQ kernel. Like the forward's key
+// split (gist.science technical summary, section 3 "Variante Split-K") it fills the GPU
+// when there are few query blocks: each split sweeps a contiguous range of
+// 64-key steps into an fp32 partial dQ, and a combine kernel sums the
+// partials. Same wave model as the forward's choice, with the dQ kernel's
+// per-step cost (~1 us at d = 128) and the partials' extra bytes.
+std::atomic<int> g_forced_dq_splits{0};  // 0: automatic
+
+int dq_steps(int NK) { return (NK + 63) / 64; }
+
+int dq_splits_auto(int B, int H, int NQ, int NK, int d, int nsets) {
+  const long long ctas = static_cast<long long>((NQ + skl::kBlockM - 1) / skl::kBlockM) * B * H;
+  const int steps = dq_steps(NK);
+  const int sms = num_sms();
+  if (ctas >= 8LL * sms) return 1;
+  const double step_us = d == 128 ? 1.0 : 0.6, cta_us = 4.0;
+  const double in_bytes = static_cast<double>(B) * H * (static_cast<double>(NK) + NQ) * d * 4.0;
+  const double part_bytes = static_cast<double>(B) * H * NQ * d * 4.0 * nsets;
+  const int smax = std::max(1, std::min(32, steps / 8));
+  auto cost = [&](int s) {
+    const long long units = ctas * s;
+    const long long waves = (units + sms - 1) / sms;
+    const long long per = (steps + s - 1) / s;
+    const double t_mma = static_cast<double>(waves) * (static_cast<double>(per) * step_us + cta_us);
+    const double streams = static_cast<double>(std::min<long long>(units, sms));
+    const double t_mem = in_bytes / std::min(7.0e12, streams * 1.0e11) * 1e6;
+    // partials written once and read once by the combine
+    const double t_comb = s > 1 ? 2.0 * s * part_bytes / 6.0e12 * 1e6 + 3.0 : 0.0;
+    return std::max(t_mma, t_mem) + t_comb;
+  };
+  int best = 1;
+  double best_t = cost(1);
+  for (int s = 2; s <= smax; ++s) {
+    const double t = cost(s);
+    if (t < best_t) {
+      best_t = t;
+      best = s;
+    }
+  }
+  if (best > 1 && best_t > 0.95 * cost(1)) return 1;
+  return best;
+}
+
+// Effective split count and key steps per split (dense batches).
+void dq_split_plan(int B, int H, int NQ, int NK, int d, int nsets, int* splits, int* per) {
+  const int forced = g_forced_dq_splits.load();
+  const int steps = dq_steps(NK);
+  const int req = forced > 0 ? forced : dq_splits_auto(B, H, NQ, NK, d, nsets);
+  const int s = std::max(1, std::min(req, steps));
+  *per = (steps + s - 1) / s;
+  *splits = (steps + *per - 1) / *per;
+}
+
+size_t dq_split_ws(int B, int H, int NQ, int NK, int d, int nsets) {
+  int splits, per;
+  dq_split_plan(B, H, NQ, NK, d, nsets, &splits, &per);
+  if (splits <= 1) return 0;
+  return align256(static_cast<size_t>(nsets) * splits * B * H * NQ * d * sizeof(float));
+}
+
 // 3-D map {d, N, B*H} of one bf16 tensor, 64-column x box_rows boxes, 128-byte swizzle.
 streamkl_status make_map(CUtensorMap* m, const void* ptr, int BH, int N, int d, const char* name,
                          int box_rows = skl::kBlockM) {
@@ -281,7 +341,25 @@ size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int caus
 
 size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
   if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return 0;
-  return bwd_ws(B, H, NQ, NK, d, want_grad1 ? 1 : 0);
+  const int g1 = want_grad1 ? 1 : 0;
+  if (bwd_algo_impl(B, H, NQ, NK, d, g1) != 0) return bwd_ws(B, H, NQ, NK, d, g1);
+  return dq_split_ws(B, H, NQ, NK, d, 1 + g1);
+}
+
+int streamkl_bwd_dq_splits(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
+  if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return -1;
+  int splits, per;
+  dq_split_plan(B, H, NQ, NK, d, want_grad1 ? 2 : 1, &splits, &per);
+  return splits;
+}
+
+int streamkl_set_bwd_dq_splits(int splits) {
+  if (splits < 0) {
+    fail(STREAMKL_ERR_INVALID_ARG, "dQ split count must be >= 0 (0: automatic)");
+    return -1;
+  }
+  g_forced_dq_splits.store(splits);
+  return 0;
 }
 
 int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
@@ -448,7 +526,12 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   // configuration 2 alone always runs the separate kernels (the fused kernel
   // always produces dQ2/dK2)
   const int algo = grad2 ? bwd_algo_impl(B, H, NQ, NK, d, grad1) : 0;
-  const size_t need = algo == 0 ? 0 : bwd_ws(B, H, NQ, NK, d, grad1);
+  // separate kernels: the dQ kernel's key split keeps its fp32 partials in
+  // the workspace; fused kernel: the fp32 dQ accumulators
+  int dq_splits = 1, dq_per = 0;
+  if (algo == 0) dq_split_plan(B, H, NQ, NK, d, grad1 + grad2, &dq_splits, &dq_per);
+  const size_t need = algo == 0 ? dq_split_ws(B, H, NQ, NK, d, grad1 + grad2)
+                                : bwd_ws(B, H, NQ, NK, d, grad1);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
     return fail(STREAMKL_ERR_INVALID_ARG, "backward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
 
@@ -475,6 +558,9 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
     a.causal = causal;
     a.grad1 = grad1;
     a.grad2 = grad2;
+    a.dq_splits = dq_splits;
+    a.dq_split_steps = dq_per;
+    a.dq_part = dq_splits > 1 ? static_cast<float*>(workspace) : nullptr;
     a.scale = scale;
     a.kl = kl;
     a.lse1 = lse1;

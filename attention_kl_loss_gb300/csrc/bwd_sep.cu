@@ -109,7 +109,8 @@ __global__ void __launch_bounds__(kSepThreads, 1)
                             int causal, float scale, const float* __restrict__ kl_in,
                             const float* __restrict__ lse1_in, const float* __restrict__ lse2_in,
                             const float* __restrict__ g_in, __nv_bfloat16* __restrict__ out2,
-                            __nv_bfloat16* __restrict__ out1, const int* __restrict__ cu_q,
+                            __nv_bfloat16* __restrict__ out1, float* __restrict__ part,
+                            int splits, int split_steps, const int* __restrict__ cu_q,
                             const int* __restrict__ cu_k, int H, int total_q, int total_k,
                             int* dev_status, uint64_t timeout_ns) {
   using L = SepLayout<D, DQ, SETS>;
@@ -144,7 +145,14 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     y_begin = causal ? max(0, x0 - off) / kStepRows : 0;
     y_end = (nq + kStepRows - 1) / kStepRows;
   }
-  int n_iter = active ? y_end - y_begin : 0;
+  // dQ kernel with a key split: this CTA takes key steps [z S, z S + S) of
+  // them (S = split_steps, z = blockIdx.z) and writes an fp32 partial dQ
+  const bool split_out = DQ && splits > 1;
+  if (split_out) {
+    y_begin = static_cast<int>(blockIdx.z) * split_steps;
+    y_end = min(y_end, y_begin + split_steps);
+  }
+  int n_iter = active ? max(0, y_end - y_begin) : 0;
 
   const uint32_t bar0 = sb + L::OFF_BAR;
   const uint32_t x_full = bar0;
@@ -469,10 +477,26 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       if (lane == 0) mbar_arrive(ds_full(it & 1));
     }
     // epilogue: accumulator row r -> bf16 dQ (dQ kernel) or dK (dK kernel)
-    // row, d columns [grp d/4, (grp+1) d/4)
+    // row, d columns [grp d/4, (grp+1) d/4); with a key split, the fp32 row
+    // of this split's partial dQ instead ([set][split][B H N_Q][d], dense
+    // batches only), zero when the split holds no key this block sees
+    constexpr int EC = D / 4;
+    auto part_row = [&](int t) {
+      const size_t plane = static_cast<size_t>(gridDim.y) * NQ;
+      return reinterpret_cast<float4*>(
+          part + ((static_cast<size_t>(t) * splits + blockIdx.z) * plane +
+                  static_cast<size_t>(sv.v_off + xrow)) * D + grp * EC);
+    };
+    if (split_out && ok && active && n_iter == 0 && xrow < NX) {
+#pragma unroll
+      for (int t = 0; t < L::NSETS; ++t) {
+        float4* dst = part_row(t);
+#pragma unroll
+        for (int i = 0; i < EC / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
     if (ok && n_iter > 0 && __all_sync(0xffffffffu, wait_bounded(acc_full, 0, wc))) {
       tc_fence_after();
-      constexpr int EC = D / 4;
 #pragma unroll
       for (int t = 0; t < L::NSETS; ++t) {
         __nv_bfloat16* out = (HAS2 && t == 0) ? out2 : out1;
@@ -483,15 +507,22 @@ __global__ void __launch_bounds__(kSepThreads, 1)
           tmem_ld16(tmem + lane_off + L::COL_ACC + t * D + grp * EC, v);
         tmem_wait_ld();
         if (xrow < NX) {
-          uint4* dst = reinterpret_cast<uint4*>(
-              out + (DQ ? sv.q_off : sv.k_off) + static_cast<long long>(xrow) * sv.row_stride +
-              grp * EC);
+          if (split_out) {
+            float4* dst = part_row(t);
 #pragma unroll
-          for (int i = 0; i < EC / 8; ++i)
-            dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]),
-                                pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                                pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
-                                pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+            for (int i = 0; i < EC / 4; ++i)
+              dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(
+                out + (DQ ? sv.q_off : sv.k_off) + static_cast<long long>(xrow) * sv.row_stride +
+                grp * EC);
+#pragma unroll
+            for (int i = 0; i < EC / 8; ++i)
+              dst[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                                  pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                                  pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                                  pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+          }
         }
       }
     }
@@ -505,6 +536,31 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   }
 }
 
+// Sum of the key splits' fp32 partial dQ rows -> bf16 dQ: one thread per 8
+// columns of one row of one gradient set; out_a is the first computed set's
+// output (dQ2 when present), out_b the second's.
+__global__ void streamkl_dq_split_combine_kernel(const float* __restrict__ part, int splits,
+                                                 long long rows, int d, int nsets,
+                                                 __nv_bfloat16* __restrict__ out_a,
+                                                 __nv_bfloat16* __restrict__ out_b) {
+  const long long per_set = rows * (d / 8);
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= per_set * nsets) return;
+  const int t = static_cast<int>(i / per_set);
+  const long long j = i - t * per_set;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < splits; ++s) {
+    const float4* p = reinterpret_cast<const float4*>(
+        part + (static_cast<size_t>(t) * splits + s) * static_cast<size_t>(rows) * d) + 2 * j;
+    const float4 a = p[0], b = p[1];
+    acc[0] += a.x, acc[1] += a.y, acc[2] += a.z, acc[3] += a.w;
+    acc[4] += b.x, acc[5] += b.y, acc[6] += b.z, acc[7] += b.w;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(t == 0 ? out_a : out_b) + j;
+  *dst = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                    pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+}
+
 template <int D, bool DQ, int SETS, bool PACKED>
 cudaError_t launch_sep_p(const BwdSepArgs& a, cudaStream_t stream) {
   using L = SepLayout<D, DQ, SETS>;
@@ -512,7 +568,8 @@ cudaError_t launch_sep_p(const BwdSepArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int NX = DQ ? a.NQ : a.NK;  // the longest sequence for packed batches
-  dim3 grid((NX + kBlockM - 1) / kBlockM, a.BH, 1);
+  const int splits = (DQ && !PACKED) ? a.dq_splits : 1;
+  dim3 grid((NX + kBlockM - 1) / kBlockM, a.BH, splits);
   const CUtensorMap* x1 = DQ ? a.tm_q1 : a.tm_k1;
   const CUtensorMap* x2 = DQ ? a.tm_q2 : a.tm_k2;
   const CUtensorMap* y1 = DQ ? a.tm_k1 : a.tm_q1;
@@ -520,8 +577,8 @@ cudaError_t launch_sep_p(const BwdSepArgs& a, cudaStream_t stream) {
   kern<<<grid, kSepThreads, L::ALLOC, stream>>>(
       *x1, *x2, *y1, *y2, a.NQ, a.NK, a.causal, a.scale, a.kl, a.lse1, a.lse2, a.g,
       static_cast<__nv_bfloat16*>(DQ ? a.dq2 : a.dk2),
-      static_cast<__nv_bfloat16*>(DQ ? a.dq1 : a.dk1), a.cu_q, a.cu_k, a.H, a.total_q, a.total_k,
-      a.dev_status, a.timeout_ns);
+      static_cast<__nv_bfloat16*>(DQ ? a.dq1 : a.dk1), splits > 1 ? a.dq_part : nullptr, splits,
+      a.dq_split_steps, a.cu_q, a.cu_k, a.H, a.total_q, a.total_k, a.dev_status, a.timeout_ns);
   return cudaGetLastError();
 }
 
@@ -548,7 +605,17 @@ size_t bwd_sep_smem_bytes(int d, int grad1) {
 cudaError_t launch_bwd_separate(const BwdSepArgs& a, cudaStream_t stream) {
   cudaError_t e = a.d == 128 ? launch_sep_g<128, false>(a, stream) : launch_sep_g<64, false>(a, stream);
   if (e != cudaSuccess) return e;
-  return a.d == 128 ? launch_sep_g<128, true>(a, stream) : launch_sep_g<64, true>(a, stream);
+  e = a.d == 128 ? launch_sep_g<128, true>(a, stream) : launch_sep_g<64, true>(a, stream);
+  if (e != cudaSuccess || a.dq_splits <= 1 || a.cu_q != nullptr) return e;
+  const int nsets = (a.grad1 ? 1 : 0) + (a.grad2 ? 1 : 0);
+  const long long rows = static_cast<long long>(a.BH) * a.NQ;
+  const long long threads = rows * (a.d / 8) * nsets;
+  const int block = 256;
+  streamkl_dq_split_combine_kernel<<<static_cast<unsigned>((threads + block - 1) / block), block, 0,
+                                     stream>>>(
+      a.dq_part, a.dq_splits, rows, a.d, nsets,
+      static_cast<__nv_bfloat16*>(a.grad2 ? a.dq2 : a.dq1), static_cast<__nv_bfloat16*>(a.dq1));
+  return cudaGetLastError();
 }
 
 }  // namespace skl

@@ -126,6 +126,11 @@ struct BwdSepArgs {
   void* dk2;
   void* dq1;  // grad1 only
   void* dk1;
+  // dQ kernel key split (dense batches): dq_splits > 1 splits the key steps
+  // into chunks of dq_split_steps; partial dQ rows go to dq_part (fp32
+  // [sets][dq_splits][BH NQ][d]) and a combine kernel sums them
+  int dq_splits = 1, dq_split_steps = 0;
+  float* dq_part = nullptr;
   int* dev_status;
   uint64_t timeout_ns;
 };

@@ -73,6 +73,9 @@ WORKLOADS = {
         # traffic and work are those of the full 32-head workload
         Workload("causal64k_h4", B=1, H=4, NQ=65536, NK=65536, d=128, causal=True, noise=0.2,
                  grad1=True),
+        # the split-K shape on 4 of its 32 heads (keys 1.07 GB, above L2):
+        # DRAM-traffic captures of the split forward
+        Workload("splitk_h4", B=4, H=4, NQ=512, NK=131072, d=128, causal=True, noise=0.1),
     ]
 }
 

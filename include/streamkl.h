@@ -74,7 +74,8 @@ size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int caus
  * section 2, kernel fusion paragraph: a fused kernel with atomic dQ updates,
  * or separate kernels when the atomics contend too much):
  *   0 = separate dK and dQ kernels: each keeps its accumulators on chip for
- *       its whole sweep; no atomics, no workspace;
+ *       its whole sweep; no atomics; a workspace only for the dQ kernel's
+ *       key split (below);
  *   1 = one fused kernel per key tile: dK on chip, dQ reduced into an fp32
  *       workspace with global atomics, then converted to bf16.
  * The automatic choice is 0: on GB300 the separate kernels measured at least
@@ -94,9 +95,30 @@ int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int 
 int streamkl_set_bwd_algorithm(int algo);
 
 /*
- * Workspace bytes the backward pass needs: 0 for the separate-kernel
- * algorithm; for the fused one, one fp32 [B, H, N_Q, d] dQ accumulator per
- * requested gradient set (two when want_grad1 != 0).
+ * Key split of the separate algorithm's dQ kernel. With few query blocks
+ * against many keys (B H ceil(N_Q/128) below 8 per SM) the dQ kernel's
+ * key range is cut into splits of 64-key steps, like the forward's split-K
+ * (gist.science technical summary, section 3 "Variante Split-K": keys
+ * partitioned across thread blocks); each split writes an fp32 partial dQ
+ * into the workspace and a
+ * combine kernel sums them into the bf16 output. Dense batches only (varlen
+ * batches never split).
+ *   streamkl_bwd_dq_splits: the split count streamkl_bwd will use for these
+ *        sizes (want_grad1 != 0: both gradient sets); -1 on invalid sizes.
+ *   streamkl_set_bwd_dq_splits: process-wide override, 0 = automatic, n >= 1
+ *        forces n splits (clamped to the number of 64-key steps); same
+ *        threading caveat as streamkl_set_bwd_algorithm. Returns 0, or -1
+ *        for a negative value.
+ */
+int streamkl_bwd_dq_splits(int B, int H, int NQ, int NK, int d, int causal, int want_grad1);
+int streamkl_set_bwd_dq_splits(int splits);
+
+/*
+ * Workspace bytes the backward pass needs, for one gradient set or, with
+ * want_grad1 != 0, both (an upper bound for configuration 2 alone): for the
+ * separate-kernel algorithm the fp32 partials of the dQ kernel's key split
+ * (0 without a split); for the fused one, one fp32 [B, H, N_Q, d] dQ
+ * accumulator per requested gradient set.
  */
 size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal,
                                    int want_grad1);
@@ -165,7 +187,7 @@ streamkl_status streamkl_fwd_noalloc(const void* q1, const void* k1, const void*
  *        dq1, dk1 likewise for configuration 2. Either pair may be NULL to
  *        skip that configuration (both of a pair NULL or neither; at least one
  *        pair is required). Configuration 2 alone always runs the separate
- *        dK/dQ kernels and needs no workspace.
+ *        dK/dQ kernels.
  *   workspace: ws_bytes >= streamkl_bwd_workspace_size(..., want_grad1) (may be
  *        NULL when that is 0); the call clears the part it uses (stream-ordered).
  */
@@ -187,9 +209,8 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
  *   streamkl_bwd_reverse: gradients of L = sum dkl * KL(P2 || P1), with kl,
  *        lse1, lse2 from streamkl_fwd_reverse. dq2, dk2 get the student's
  *        gradients (P1 fixed), dq1, dk1 the teacher's (P2 fixed); either pair
- *        may be NULL to skip it (at least one pair). With the teacher pair
- *        NULL no workspace is needed; ws_bytes >= streamkl_bwd_workspace_size(
- *        ..., want_grad1 = 1) always suffices.
+ *        may be NULL to skip it (at least one pair). ws_bytes >=
+ *        streamkl_bwd_workspace_size(..., want_grad1 = both pairs requested).
  * Errors as for streamkl_fwd / streamkl_bwd; a message about a tensor names
  * it by its slot in the exchanged call (q1 for the q2 given here, and so on).
  */

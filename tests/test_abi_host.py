@@ -72,10 +72,15 @@ def test_workspace_sizes(lib):
         assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 0) == 32 * 65536 * 128 * 4
         assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == max(
             5 * s * 128 * 512 * 4, 128 * 512 * 128 * 4)
-        assert lib.streamkl_set_bwd_algorithm(0) == 0  # separate: no workspace
+        # separate: only the dQ kernel's key-split partials
+        assert lib.streamkl_set_bwd_algorithm(0) == 0
         assert lib.streamkl_bwd_algorithm(1, 32, 65536, 65536, 128, 1, 1) == 0
         assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 1) == 0
-        assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 5 * s * 128 * 512 * 4
+        dq = lib.streamkl_bwd_dq_splits(4, 32, 512, 131072, 128, 1, 0)
+        dq_ws = dq * 128 * 512 * 128 * 4 if dq > 1 else 0
+        assert lib.streamkl_bwd_workspace_size(4, 32, 512, 131072, 128, 1, 0) == dq_ws
+        assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == max(
+            5 * s * 128 * 512 * 4, dq_ws)
         assert lib.streamkl_set_bwd_algorithm(7) == -1
     finally:
         lib.streamkl_set_bwd_algorithm(-1)
@@ -88,7 +93,29 @@ def test_automatic_backward_choice(lib):
                  (4, 32, 512, 131072, 128, 1, 0), (4, 32, 256, 65536, 128, 1, 0),
                  (4, 32, 512, 131072, 64, 1, 0)]:
         assert lib.streamkl_bwd_algorithm(*args) == 0, args
-    assert lib.streamkl_bwd_workspace_size(4, 32, 512, 131072, 128, 1, 0) == 0
+
+
+def test_dq_key_split_choice(lib):
+    """The separate backward's dQ kernel splits its keys only when there are
+    few query blocks: never at 64K (16,384 dQ CTAs), at least 2 ways for the
+    split-K shape (512 CTAs, 3.4 waves on 152 SMs) and for one query block per
+    head; the split partials' workspace follows the count, forced or not."""
+    lib.streamkl_set_bwd_dq_splits(0)
+    assert lib.streamkl_bwd_dq_splits(1, 32, 65536, 65536, 128, 1, 1) == 1
+    assert lib.streamkl_bwd_dq_splits(4, 32, 512, 131072, 128, 1, 0) >= 2
+    assert lib.streamkl_bwd_dq_splits(1, 4, 128, 131072, 128, 1, 0) >= 8
+    assert lib.streamkl_bwd_dq_splits(1, 1, 8, 4, 64, 1, 0) == -1  # invalid sizes
+    try:
+        assert lib.streamkl_set_bwd_dq_splits(3) == 0
+        # 200 keys = 4 steps of 64: 3 requested -> 2 steps each -> 2 splits
+        assert lib.streamkl_bwd_dq_splits(1, 1, 100, 200, 64, 0, 0) == 2
+        assert lib.streamkl_bwd_workspace_size(1, 1, 100, 200, 64, 0, 0) == 2 * 100 * 64 * 4
+        assert lib.streamkl_bwd_workspace_size(1, 1, 100, 200, 64, 0, 1) == 2 * 2 * 100 * 64 * 4
+        assert lib.streamkl_bwd_dq_splits(1, 1, 8, 8, 64, 0, 0) == 1  # one step: no split
+        assert lib.streamkl_bwd_workspace_size(1, 1, 8, 8, 64, 0, 0) == 0
+        assert lib.streamkl_set_bwd_dq_splits(-1) == -1
+    finally:
+        lib.streamkl_set_bwd_dq_splits(0)
 
 
 def test_forced_split_workspace_rounding(lib):

@@ -189,6 +189,47 @@ def test_configuration2_only(NQ, NK, d, causal):
             assert_grad(host(only[3][b, hh]), og[3], "dk1")
 
 
+@pytest.mark.parametrize("splits", [1, 2, 3, 5])
+@pytest.mark.parametrize("NQ,NK,d,causal,sets", [
+    (200, 2000, 128, True, "both"),    # few query blocks, long keys, ragged
+    (130, 1500, 64, False, "config1"),
+    (640, 700, 128, True, "config2"),  # late splits hold no key of the early blocks
+])
+def test_dq_key_split(NQ, NK, d, causal, sets, splits):
+    """The separate backward's dQ kernel with its keys split (fp32 partials
+    summed by the combine kernel) against the oracle, for forced split counts;
+    dK is unaffected. Covers splits that see no key of a query block (their
+    partial rows are zeros) and the combine's mapping of one or two sets."""
+    w = synthetic.custom(f"dqsplit_{NQ}x{NK}d{d}", B=1, H=2, NQ=NQ, NK=NK, d=d, causal=causal,
+                         noise=0.5, grad1=sets != "config1")
+    dev = torch.device("cuda")
+    ins = synthetic.make_inputs(w, 13, dev)
+    q1, k1, q2, k2, g = ins
+    status = binding.new_status(dev)
+    kl, lse1, lse2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, dev_status=status)
+    binding.set_bwd_algorithm(binding.BWD_SEPARATE)
+    binding.set_bwd_dq_splits(splits)
+    try:
+        steps = (NK + 63) // 64  # 64-key steps; each split takes ceil(steps / splits)
+        per = -(-steps // min(splits, steps))
+        assert binding.bwd_dq_splits(w.B, w.H, NQ, NK, d, causal, sets == "both") == -(-steps // per)
+        grads = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                     grad1=sets != "config1", grad2=sets != "config2",
+                                     dev_status=status)
+    finally:
+        binding.set_bwd_dq_splits(None)
+        binding.set_bwd_algorithm(None)
+    binding.raise_on_device_status(status, "dQ key split")
+    for hh in range(w.H):
+        h = [host(t[0, hh]) for t in ins[:4]]
+        og = orc.head_backward(*h, w.scale, w.causal, g[0, hh].cpu().numpy().astype(np.float64),
+                               True)
+        for i, name in enumerate(["dq2", "dk2", "dq1", "dk1"]):
+            if grads[i] is None:
+                continue
+            assert_grad(host(grads[i][0, hh]), og[i], name)
+
+
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("NQ,NK,d,causal", [(256, 256, 64, False), (200, 333, 128, True)])
 def test_reverse_direction(NQ, NK, d, causal, algo):
