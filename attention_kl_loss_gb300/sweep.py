@@ -3,6 +3,7 @@
     python -m attention_kl_loss_gb300.sweep algo      # fused vs separate backward
     python -m attention_kl_loss_gb300.sweep decode    # split-K on/off for few query rows
     python -m attention_kl_loss_gb300.sweep context   # context length 4K .. 512K
+    python -m attention_kl_loss_gb300.sweep dqsplit   # backward dQ key split on/off
 
 Every point is timed through the C ABI with CUDA events on the current stream,
 inputs resident in device memory, one untimed call first, the median of
@@ -103,6 +104,39 @@ def sweep_decode(reps: int):
             torch.cuda.empty_cache()
 
 
+def sweep_dqsplit(reps: int):
+    """Separate backward with the dQ kernel's key split forced off and at the
+    library's choice, on shapes with few query blocks against long keys."""
+    dev = torch.device("cuda")
+    shapes = [synthetic.WORKLOADS["splitk"], synthetic.WORKLOADS["splitk_h4"]] + [
+        synthetic.custom(f"q{nq}_k{nk // 1024}k_b{b}h{h}", B=b, H=h, NQ=nq, NK=nk, d=d, causal=True,
+                         noise=0.1, grad1=g1)
+        for (b, h, nq, nk, d, g1) in [(1, 8, 512, 131072, 128, False), (1, 32, 1024, 65536, 128, True),
+                                      (4, 32, 256, 65536, 128, False), (4, 32, 64, 65536, 128, False),
+                                      (1, 8, 512, 131072, 64, False)]]
+    print("| workload | sets | splits chosen | ms, no split | ms, chosen | speed-up |")
+    print("|---|---|---:|---:|---:|---:|")
+    for w in shapes:
+        (q1, k1, q2, k2, g), st = _setup(w, dev)
+        kl, l1, l2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, dev_status=st)
+        res = {}
+        for forced in (1, None):
+            binding.set_bwd_dq_splits(forced)
+            try:
+                res[forced] = _time(lambda: binding.streamkl_bwd(
+                    q1, k1, q2, k2, kl, l1, l2, g, w.scale, w.causal, grad1=w.grad1,
+                    dev_status=st), reps)
+            finally:
+                binding.set_bwd_dq_splits(None)
+        _check(st, w.name)
+        s = binding.bwd_dq_splits(w.B, w.H, w.NQ, w.NK, w.d, w.causal, w.grad1)
+        print(f"| {w.name} (B{w.B} H{w.H} {w.NQ}x{w.NK} d{w.d} causal) | "
+              f"{'both' if w.grad1 else 'config 1'} | {s} | {res[1]:.3f} | {res[None]:.3f} | "
+              f"{res[1] / res[None]:.2f} |")
+        del q1, k1, q2, k2, g
+        torch.cuda.empty_cache()
+
+
 def sweep_context(reps: int):
     """Causal fwd + bwd (both sets) from 4K to 512K: time and extra device memory."""
     dev = torch.device("cuda")
@@ -137,11 +171,12 @@ def sweep_context(reps: int):
 
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    p.add_argument("what", choices=["algo", "decode", "context"])
+    p.add_argument("what", choices=["algo", "decode", "context", "dqsplit"])
     p.add_argument("--reps", type=int, default=3)
     a = p.parse_args(argv)
     binding.load()
-    {"algo": sweep_algo, "decode": sweep_decode, "context": sweep_context}[a.what](a.reps)
+    {"algo": sweep_algo, "decode": sweep_decode, "context": sweep_context,
+     "dqsplit": sweep_dqsplit}[a.what](a.reps)
 
 
 if __name__ == "__main__":
