@@ -13,7 +13,9 @@
 // seen from the X side (S_t in the dQ kernel, S_t^T in the dK kernel), the
 // softmax warps turn T1, T2 into the matching dS tiles and the gradient GEMM
 // is acc_t += dT_t Y_t (M = 128, N = d, K = 64), accumulated in TMEM over the
-// whole sweep and written out once.
+// whole sweep and written out once. With few query blocks the dQ kernel
+// also splits its keys across CTAs (grid z): each split writes its
+// accumulator as an fp32 partial and a combine kernel sums the partials.
 //
 // dS never goes through shared memory: each softmax thread owns one X row,
 // which is one TMEM lane, so it stores its bf16 dS values straight into TMEM
