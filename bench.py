@@ -10,8 +10,9 @@ Metric: fwd+bwd TFLOP/s at that workload with the usual attention convention,
 The value is device-timed with inputs resident in HBM (inputs are 2 GiB, far
 larger than the 129 MB L2, so no flush is needed between steps). ``e2e`` is
 the same metric through the public Python API with host (pinned) buffers:
-each step copies the inputs in and the per-row KL out (step k+1's copy
-runs on a second stream during step k's compute).
+each step copies the inputs in and the per-row KL out (the batch streamed in
+groups of heads: a group's copy runs on a second stream while the previous
+group computes).
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
 bounded sample of the same workload per step).
@@ -443,25 +444,37 @@ def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
     """Same metric through the public API with host buffers: every step copies
     its inputs from pinned host memory and reads the per-row KL back.
 
-    The device inputs are double-buffered: step k+1's host-to-device copy runs
-    on a second stream while step k computes, so only the first step's copy is
-    exposed. Every step's copy is enqueued after the start event and finishes
-    before the step that uses it, so all of them fall inside the timed region."""
+    A step's batch goes through the API in G groups of (batch, head) slices
+    (heads are independent, so this is the same computation), streamed
+    through two device buffers: group i+1's host-to-device copy runs on a
+    second stream while group i computes, so only the first group's copy of
+    the first step is exposed. Every copy is enqueued after the start event
+    and finishes before the group that uses it, so all of them fall inside
+    the timed region."""
     import torch
     q1, k1, q2, k2, g = synthetic.make_inputs(w, replica_seed(rank) + 7, dev)
     host_in = [t.cpu().pin_memory() for t in (q1, k1, q2, k2, g)]
     del q1, k1, q2, k2, g
-    bufs = [[torch.empty_like(t, device=dev) for t in host_in] for _ in range(2)]
+    bh = w.B * w.H
+    groups = next(c for c in (4, 2, 1) if bh % c == 0)
+    per = bh // groups
+
+    def part(t, i):  # slices [i per, (i+1) per) of the flattened (batch, head) axis, as [1, per, ...]
+        return t.reshape((bh,) + tuple(t.shape[2:]))[i * per:(i + 1) * per].unsqueeze(0)
+
+    host_groups = [[part(t, i) for t in host_in] for i in range(groups)]
+    bufs = [[torch.empty_like(t, device=dev) for t in host_groups[0]] for _ in range(2)]
     kl_host = torch.empty((w.B, w.H, w.NQ), dtype=torch.float32).pin_memory()
+    kl_groups = [part(kl_host, i) for i in range(groups)]
     stream = torch.cuda.current_stream(dev)
     copy_stream = torch.cuda.Stream(dev)
     ready = [torch.cuda.Event() for _ in range(2)]
     free = [torch.cuda.Event() for _ in range(2)]
 
-    def h2d(slot):
+    def h2d(slot, gi):
         with torch.cuda.stream(copy_stream):
             copy_stream.wait_event(free[slot])
-            for hsrc, d in zip(host_in, bufs[slot]):
+            for hsrc, d in zip(host_groups[gi], bufs[slot]):
                 d.copy_(hsrc, non_blocking=True)
             ready[slot].record(copy_stream)
 
@@ -469,17 +482,18 @@ def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
         for e in free:
             e.record(stream)
         copy_stream.wait_stream(stream)
-        h2d(0)
-        for s in range(steps):
-            slot = s & 1
-            if s + 1 < steps:
-                h2d(slot ^ 1)
+        units = steps * groups
+        h2d(0, 0)
+        for u in range(units):
+            slot, gi = u & 1, u % groups
+            if u + 1 < units:
+                h2d(slot ^ 1, (u + 1) % groups)
             stream.wait_event(ready[slot])
             x = bufs[slot]
             kl, l1, l2 = binding.streamkl_fwd(*x[:4], w.scale, w.causal)
             binding.streamkl_bwd(*x[:4], kl, l1, l2, x[4], w.scale, w.causal, grad1=w.grad1)
             free[slot].record(stream)
-            kl_host.copy_(kl, non_blocking=True)
+            kl_groups[gi].copy_(kl, non_blocking=True)
 
     run(max(1, args.warmup))
     torch.cuda.synchronize(dev)
@@ -495,8 +509,9 @@ def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
     d2h = kl_host.numel() * 4
     return {"value": world * step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h,
-            "overlap": "inputs double-buffered: step k+1's host-to-device copy runs on a second "
-                       "stream during step k; the first step's copy is exposed",
+            "overlap": f"each step's batch in {groups} groups of {per} (batch, head) slices through "
+                       "two device buffers: a group's host-to-device copy runs on a second stream "
+                       "while the previous group computes; the first group's copy is exposed",
             "api": "attention_kl_loss_gb300.streamkl_fwd/streamkl_bwd (ctypes over the C ABI)"}
 
 
