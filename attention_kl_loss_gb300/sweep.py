@@ -4,6 +4,7 @@
     python -m attention_kl_loss_gb300.sweep decode    # split-K on/off for few query rows
     python -m attention_kl_loss_gb300.sweep context   # context length 4K .. 512K
     python -m attention_kl_loss_gb300.sweep dqsplit   # backward dQ key split on/off
+    python -m attention_kl_loss_gb300.sweep configs   # the named workloads, fwd and bwd
 
 Every point is timed through the C ABI with CUDA events on the current stream,
 inputs resident in device memory, one untimed call first, the median of
@@ -137,6 +138,44 @@ def sweep_dqsplit(reps: int):
         torch.cuda.empty_cache()
 
 
+def sweep_configs(reps: int):
+    """Forward and backward of every named workload at the library's choices,
+    with the exact visible-pair FLOP counts: 4d per pair forward; the
+    separate backward executes 12d per pair with one gradient set (each of
+    its two kernels recomputes both score tiles, 4d, and runs one gradient
+    GEMM, 2d) and 16d with both."""
+    import json
+    import os
+    dev = torch.device("cuda")
+    peak = None
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            peak = json.load(f).get("bf16_tflops_sustained")
+    print("| workload | sets | fwd ms | bwd ms | fwd TFLOP/s | bwd TFLOP/s executed | "
+          f"fwd / bwd of {'measured sustained peak' if peak else 'peak (not available)'} |")
+    print("|---|---|---:|---:|---:|---:|---|")
+    for name in ("tiny", "mid", "causal64k", "splitk", "stress"):
+        w = synthetic.WORKLOADS[name]
+        (q1, k1, q2, k2, g), st = _setup(w, dev)
+        out = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, dev_status=st)
+        tf = _time(lambda: binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, out=out,
+                                                dev_status=st), reps)
+        kl, l1, l2 = out
+        tb = _time(lambda: binding.streamkl_bwd(q1, k1, q2, k2, kl, l1, l2, g, w.scale, w.causal,
+                                                grad1=w.grad1, dev_status=st), reps)
+        _check(st, name)
+        pairs = w.live_pairs_per_head() * w.B * w.H
+        ff = 4 * w.d * pairs / tf / 1e9
+        fb = (16 if w.grad1 else 12) * w.d * pairs / tb / 1e9
+        frac = f"{ff / peak:.2f} / {fb / peak:.2f}" if peak else "-"
+        print(f"| {name} (B{w.B} H{w.H} {w.NQ}x{w.NK} d{w.d}{' causal' if w.causal else ''}) | "
+              f"{'both' if w.grad1 else 'config 1'} | {tf:.3f} | {tb:.3f} | {ff:.0f} | {fb:.0f} | {frac} |")
+        del q1, k1, q2, k2, g
+        torch.cuda.empty_cache()
+
+
 def sweep_context(reps: int):
     """Causal fwd + bwd (both sets) from 4K to 512K: time and extra device memory."""
     dev = torch.device("cuda")
@@ -171,12 +210,12 @@ def sweep_context(reps: int):
 
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    p.add_argument("what", choices=["algo", "decode", "context", "dqsplit"])
+    p.add_argument("what", choices=["algo", "decode", "context", "dqsplit", "configs"])
     p.add_argument("--reps", type=int, default=3)
     a = p.parse_args(argv)
     binding.load()
     {"algo": sweep_algo, "decode": sweep_decode, "context": sweep_context,
-     "dqsplit": sweep_dqsplit}[a.what](a.reps)
+     "dqsplit": sweep_dqsplit, "configs": sweep_configs}[a.what](a.reps)
 
 
 if __name__ == "__main__":
