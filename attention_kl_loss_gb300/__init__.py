@@ -10,6 +10,7 @@ from .binding import (  # noqa: F401
     BWD_SEPARATE,
     StreamKLError,
     bwd_algorithm,
+    bwd_dk_persist,
     bwd_dq_splits,
     choose_splits,
     load,
@@ -17,6 +18,7 @@ from .binding import (  # noqa: F401
     raise_on_device_status,
     selftest_wait_timeout,
     set_bwd_algorithm,
+    set_bwd_dk_persist,
     set_bwd_dq_splits,
     streamkl_bwd,
     streamkl_bwd_reverse,

@@ -49,6 +49,8 @@ _SIGNATURES = {
     "streamkl_set_bwd_algorithm": (_I, [_I]),
     "streamkl_bwd_dq_splits": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "streamkl_set_bwd_dq_splits": (_I, [_I]),
+    "streamkl_bwd_dk_persist": (_I, [_I, _I, _I, _I, _I, _I]),
+    "streamkl_set_bwd_dk_persist": (_I, [_I]),
     "streamkl_fwd_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P,
                                   _P, _P]),
     "streamkl_fwd_varlen": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I,
@@ -150,6 +152,17 @@ def set_bwd_dq_splits(splits: Optional[int]) -> None:
     """Force the dQ kernel's key splits (None or 0: automatic)."""
     if load().streamkl_set_bwd_dq_splits(0 if splits is None else int(splits)) != 0:
         raise ValueError(f"invalid dQ split count {splits!r}")
+
+
+def bwd_dk_persist(B, H, NQ, NK, d, causal) -> int:
+    """Persistent dK CTAs the backward launches for these sizes (0: none)."""
+    return int(load().streamkl_bwd_dk_persist(B, H, NQ, NK, d, int(causal)))
+
+
+def set_bwd_dk_persist(ctas: Optional[int]) -> None:
+    """Force the persistent dK kernel (n CTAs), turn it off (-1), or None/0: automatic."""
+    if load().streamkl_set_bwd_dk_persist(0 if ctas is None else int(ctas)) != 0:
+        raise ValueError(f"invalid persistent dK CTA count {ctas!r}")
 
 
 def set_bwd_algorithm(algo: Optional[int]) -> None:

@@ -101,8 +101,12 @@ __device__ __forceinline__ float4 query_const(const float* lse1, const float* ls
 
 // PACKED: a variable-length batch of packed sequences instead of dense
 // [B, H, N, d] tensors; a template parameter so that the dense kernel keeps
-// its sizes as kernel parameters.
-template <int D, bool DQ, int SETS, bool PACKED>
+// its sizes as kernel parameters. PERSIST (dK kernel, dense batches): each
+// CTA takes (key block, batch-head) items round-robin, heavy key blocks
+// first, and loads the next item's X as soon as the last T GEMMs of the
+// current one have read X; for short query sweeps, where a CTA's fixed start
+// and end would otherwise weigh.
+template <int D, bool DQ, int SETS, bool PACKED, bool PERSIST>
 __global__ void __launch_bounds__(kSepThreads, 1)
     streamkl_bwd_sep_kernel(const __grid_constant__ CUtensorMap tm_x1,
                             const __grid_constant__ CUtensorMap tm_x2,
@@ -112,49 +116,73 @@ __global__ void __launch_bounds__(kSepThreads, 1)
                             const float* __restrict__ lse1_in, const float* __restrict__ lse2_in,
                             const float* __restrict__ g_in, __nv_bfloat16* __restrict__ out2,
                             __nv_bfloat16* __restrict__ out1, float* __restrict__ part,
-                            int splits, int split_steps, const int* __restrict__ cu_q,
+                            int splits, int split_steps, int n_bh, const int* __restrict__ cu_q,
                             const int* __restrict__ cu_k, int H, int total_q, int total_k,
                             int* dev_status, uint64_t timeout_ns) {
   using L = SepLayout<D, DQ, SETS>;
   constexpr bool HAS2 = SETS & kSet2, HAS1 = SETS & kSet1;
+  static_assert(!PERSIST || (!DQ && !PACKED), "persistent: dense dK kernel only");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sb = (raw + 1023u) & ~1023u;
   uint8_t* gb = smem_raw + (sb - raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  const int bh = static_cast<int>(blockIdx.y);
-  // this (batch, head) slice: the whole tensor's sizes, or one sequence of a
-  // packed variable-length batch (the grid covers the longest one)
-  const SeqView sv = PACKED ? seq_view_packed(bh, H, NQ, NK, D, cu_q, cu_k, total_q, total_k)
-                            : seq_view_dense(bh, NQ, NK, D);
-  const int nq = sv.nq, nk = sv.nk;
-  const int NX = DQ ? nq : nk;
-  const int nxb = (NX + kBlockM - 1) / kBlockM;
-  const bool active = sv.ok && static_cast<int>(blockIdx.x) < nxb && !(causal && nq > nk);
-  const int off = nk - nq;  // key j is visible to query i iff j <= i + off (causal)
-  // causal: the dQ kernel's heavy blocks are the last query blocks, the dK
-  // kernel's the first key blocks; launch the heavy ones first
-  const int xb = (DQ && causal) ? nxb - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
-  const int x0 = xb * kBlockM;
-  const int x_row0 = DQ ? sv.q_row0 : sv.k_row0, y_row0 = DQ ? sv.k_row0 : sv.q_row0;
-  int y_begin, y_end;  // in steps of 64 Y rows
-  if (DQ) {  // key steps visible to some row of this query block
-    const int klim = causal ? min(nk, min(nq, x0 + kBlockM) + off) : nk;
-    y_begin = 0;
-    y_end = (klim + kStepRows - 1) / kStepRows;
-  } else {  // query steps with a row that sees some key of this block
-    y_begin = causal ? max(0, x0 - off) / kStepRows : 0;
-    y_end = (nq + kStepRows - 1) / kStepRows;
-  }
-  // dQ kernel with a key split: this CTA takes key steps [z S, z S + S) of
-  // them (S = split_steps, z = blockIdx.z) and writes an fp32 partial dQ
+  // One work item: an X block of one (batch, head) slice (and, dQ kernel with
+  // a key split, one range of key steps).
+  struct Item {
+    SeqView sv;
+    int nq, nk, NX, off, x0, x_row0, y_row0, y_begin, n_iter;
+    bool active;
+  };
+  auto make_item = [&](int bx, int bh, int bz) {
+    Item I;
+    // this (batch, head) slice: the whole tensor's sizes, or one sequence of a
+    // packed variable-length batch (the grid covers the longest one)
+    I.sv = PACKED ? seq_view_packed(bh, H, NQ, NK, D, cu_q, cu_k, total_q, total_k)
+                  : seq_view_dense(bh, NQ, NK, D);
+    I.nq = I.sv.nq;
+    I.nk = I.sv.nk;
+    I.NX = DQ ? I.nq : I.nk;
+    const int nxb = (I.NX + kBlockM - 1) / kBlockM;
+    I.active = I.sv.ok && bx < nxb && !(causal && I.nq > I.nk);
+    I.off = I.nk - I.nq;  // key j is visible to query i iff j <= i + off (causal)
+    // causal: the dQ kernel's heavy blocks are the last query blocks, the dK
+    // kernel's the first key blocks; launch the heavy ones first
+    const int xb = (DQ && causal) ? nxb - 1 - bx : bx;
+    I.x0 = xb * kBlockM;
+    I.x_row0 = DQ ? I.sv.q_row0 : I.sv.k_row0;
+    I.y_row0 = DQ ? I.sv.k_row0 : I.sv.q_row0;
+    int y_end;  // in steps of 64 Y rows
+    if (DQ) {  // key steps visible to some row of this query block
+      const int klim = causal ? min(I.nk, min(I.nq, I.x0 + kBlockM) + I.off) : I.nk;
+      I.y_begin = 0;
+      y_end = (klim + kStepRows - 1) / kStepRows;
+    } else {  // query steps with a row that sees some key of this block
+      I.y_begin = causal ? max(0, I.x0 - I.off) / kStepRows : 0;
+      y_end = (I.nq + kStepRows - 1) / kStepRows;
+    }
+    // dQ kernel with a key split: this CTA takes key steps [z S, z S + S) of
+    // them (S = split_steps, z = blockIdx.z) and writes an fp32 partial dQ
+    if (DQ && splits > 1) {
+      I.y_begin = bz * split_steps;
+      y_end = min(y_end, I.y_begin + split_steps);
+    }
+    I.n_iter = I.active ? max(0, y_end - I.y_begin) : 0;
+    return I;
+  };
   const bool split_out = DQ && splits > 1;
-  if (split_out) {
-    y_begin = static_cast<int>(blockIdx.z) * split_steps;
-    y_end = min(y_end, y_begin + split_steps);
-  }
-  int n_iter = active ? max(0, y_end - y_begin) : 0;
+  // items: one per CTA, or (persistent) item i = key block i / n_bh of slice
+  // i % n_bh for i = blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int n_items = PERSIST ? ((NK + kBlockM - 1) / kBlockM) * n_bh : 1;
+  const int item_stride = PERSIST ? static_cast<int>(gridDim.x) : 1;
+  const int item_first = PERSIST ? static_cast<int>(blockIdx.x) : 0;
+  auto item_at = [&](int i) {
+    return PERSIST ? make_item(i / n_bh, i % n_bh, 0)
+                   : make_item(static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y),
+                               static_cast<int>(blockIdx.z));
+  };
+  const Item I0 = item_at(item_first);
 
   const uint32_t bar0 = sb + L::OFF_BAR;
   const uint32_t x_full = bar0;
@@ -168,6 +196,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   auto ds_free = [&](int b) { return s_full + 32 + 8u * b; };
   const uint32_t acc_full = s_full + 48;
   const uint32_t drain = s_full + 56;
+  // persistent: X of the next item may be loaded; the accumulators were read
+  const uint32_t x_free = s_full + 64;
+  const uint32_t acc_empty = s_full + 72;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
   volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
@@ -191,12 +222,14 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     }
     mbar_init(acc_full, 1);
     mbar_init(drain, 2);  // one commit per MMA-issuing thread
+    mbar_init(x_free, 1);
+    mbar_init(acc_empty, kSoftmaxWarps);
     *abort_flag = 0;
     // a failure recorded earlier (this launch or a previous one) skips the work
     *skip_flag = *reinterpret_cast<volatile int*>(dev_status) != 0;
     // malformed sequence offsets, or a causal sequence with more query rows
     // than keys: reported, never computed
-    if (!sv.ok || (causal && nq > nk)) atomicCAS(dev_status, 0, kStatusInvalidArg);
+    if (!I0.sv.ok || (causal && I0.nq > I0.nk)) atomicCAS(dev_status, 0, kStatusInvalidArg);
     *t_queued = 0;
     fence_mbar_init();
   }
@@ -214,38 +247,54 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (*skip_flag) n_iter = 0;
+  const bool skip = *skip_flag;
   const WaitCtx wc{abort_flag, dev_status, timeout_ns};
+  // the items of this CTA in order; steps are numbered globally across them
+  // (g = steps of the earlier items) for the Y ring and the per-step barriers
+  auto item_steps = [&](const Item& I) { return skip ? 0 : I.n_iter; };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (n_iter > 0) {
+    bool ok = true;
+    int g = 0, ic = 0, n_x = 0;  // steps so far, items so far, X loads issued
+    for (int item = item_first; ok && item < n_items; item += item_stride) {
+      const Item I = item == item_first ? I0 : item_at(item);
+      const int n = item_steps(I);
+      if (n == 0) continue;
       if (lane == 0) {
-        mbar_arrive_expect_tx(x_full, 2 * L::XT);
+        // persistent: the previous item's T GEMMs have read X
+        if (ic > 0) ok = wait_bounded(x_free, (ic - 1) & 1, wc);
+        if (ok) {
+          mbar_arrive_expect_tx(x_full, 2 * L::XT);
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int b = 0; b < L::KB; ++b)
+            for (int b = 0; b < L::KB; ++b)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tma_load_3d(sb + L::OFF_X + t * L::XT + b * 16384 + h * 8192, t == 0 ? &tm_x1 : &tm_x2,
-                          x_full, b * 64, x_row0 + x0 + h * kStepRows, sv.z);
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d(sb + L::OFF_X + t * L::XT + b * 16384 + h * 8192,
+                            t == 0 ? &tm_x1 : &tm_x2, x_full, b * 64,
+                            I.x_row0 + I.x0 + h * kStepRows, I.sv.z);
+          ++n_x;
+        }
       }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
       auto qv = [&](int q) {  // per-row vector element of query row q
-        return static_cast<size_t>(sv.v_off + static_cast<long long>(q) * sv.v_stride);
+        return static_cast<size_t>(I.sv.v_off + static_cast<long long>(q) * I.sv.v_stride);
       };
       int it = 0;
-      for (; it < n_iter; ++it) {
-        const int s = it % kStages;
-        const int yrow = (y_begin + it) * kStepRows;
+      for (; it < n; ++it) {
+        const int G = g + it;
+        const int s = G % kStages;
+        const int yrow = (I.y_begin + it) * kStepRows;
         float4 c0, c1;  // dK kernel: this lane's two table entries, loaded before the wait
         if (!DQ) {
-          c0 = query_const(lse1_in, lse2_in, g_in, kl_in, qv(yrow + lane), scale, yrow + lane < nq);
+          c0 = query_const(lse1_in, lse2_in, g_in, kl_in, qv(yrow + lane), scale, yrow + lane < I.nq);
           c1 = query_const(lse1_in, lse2_in, g_in, kl_in, qv(yrow + lane + 32), scale,
-                           yrow + lane + 32 < nq);
+                           yrow + lane + 32 < I.nq);
         }
         bool good = true;
-        if (lane == 0) good = wait_bounded(y_empty(s), ((it / kStages) & 1) ^ 1, wc);
+        if (lane == 0) good = wait_bounded(y_empty(s), ((G / kStages) & 1) ^ 1, wc);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (!DQ) {
           float* ts = tab + s * 4 * kStepRows;
@@ -263,31 +312,34 @@ __global__ void __launch_bounds__(kSepThreads, 1)
 #pragma unroll
             for (int b = 0; b < L::KB; ++b)
               tma_load_3d(dst + t * L::YT + b * 8192, t == 0 ? &tm_y1 : &tm_y2, y_full(s), b * 64,
-                          y_row0 + yrow, sv.z);
+                          I.y_row0 + yrow, I.sv.z);
         }
       }
-      // let every copy this thread issued land before the CTA can exit
-      if (lane == 0) {
-        wait_drain(x_full, 0, timeout_ns);
-        for (int j = max(0, it - kStages); j < it; ++j)
-          wait_drain(y_full(j % kStages), (j / kStages) & 1, timeout_ns);
-      }
+      g += it;
+      ++ic;
+      if (it < n) ok = false;
+    }
+    // let every copy this thread issued land before the CTA can exit
+    if (lane == 0) {
+      if (n_x > 0) wait_drain(x_full, (n_x - 1) & 1, timeout_ns);
+      for (int j = max(0, g - kStages); j < g; ++j)
+        wait_drain(y_full(j % kStages), (j / kStages) & 1, timeout_ns);
     }
   } else if (warp == 1 || warp == kGradWarp) {
     // ------------------------------------------------------------ MMA issuers
     // Warp 1 issues the T GEMMs, warp 18 the gradient GEMMs: each one's waits
     // overlap the other's MMAs in the tensor pipe. A thread's commit tracks
     // only the MMAs that thread issued.
-    if (lane == 0 && n_iter > 0) {
+    if (lane == 0 && (PERSIST || item_steps(I0) > 0)) {
       constexpr uint32_t id_t = idesc_bf16(kBlockM, kStepRows, 0, 0);
       constexpr uint32_t id_g = idesc_bf16(kBlockM, D, 0, 1);
       const uint32_t x1 = sb + L::OFF_X, x2 = x1 + L::XT;
       // Descriptors are built once per stage and advanced by compile-time
       // offsets, so issuing an MMA costs two adds.
       const uint64_t dx1 = smem_desc_sw128(x1, 16, 1024), dx2 = smem_desc_sw128(x2, 16, 1024);
-      // T = X Y^T of step st (two K-major GEMMs, k-steps interleaved)
-      auto issue_t = [&](int st) {
-        const uint64_t dy = smem_desc_sw128(sb + L::OFF_Y + (st % kStages) * 2 * L::YT, 16, 1024);
+      // T = X Y^T of global step G (two K-major GEMMs, k-steps interleaved)
+      auto issue_t = [&](int G) {
+        const uint64_t dy = smem_desc_sw128(sb + L::OFF_Y + (G % kStages) * 2 * L::YT, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t xo = (k >> 2) * 16384 + (k & 3) * 32, yo = (k >> 2) * 8192 + (k & 3) * 32;
@@ -297,12 +349,13 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         }
         mma_commit(s_full);
       };
-      // gradient GEMMs of step j: A = dS from TMEM buffer j&1 (slot t of a
-      // buffer holds the t-th computed set), B = the set's Y (set 2: Y2, set
-      // 1: Y1) MN-major; with two sets their k-steps interleave
-      auto issue_g = [&](int j) {
-        const uint64_t dy = smem_desc_sw128(sb + L::OFF_Y + (j % kStages) * 2 * L::YT, 8192, 1024);
-        const uint32_t dsb = tmem + L::COL_DS + (j & 1) * 64;
+      // gradient GEMMs of global step G (step j of its item): A = dS from TMEM
+      // buffer G&1 (slot t of a buffer holds the t-th computed set), B = the
+      // set's Y (set 2: Y2, set 1: Y1) MN-major; with two sets their k-steps
+      // interleave; the item's first step starts the accumulators
+      auto issue_g = [&](int G, int j) {
+        const uint64_t dy = smem_desc_sw128(sb + L::OFF_Y + (G % kStages) * 2 * L::YT, 8192, 1024);
+        const uint32_t dsb = tmem + L::COL_DS + (G & 1) * 64;
 #pragma unroll
         for (int kg = 0; kg < 4; ++kg)
 #pragma unroll
@@ -311,42 +364,62 @@ __global__ void __launch_bounds__(kSepThreads, 1)
             mma_bf16_ts(tmem + L::COL_ACC + t * D, dsb + 32 * t + 8 * kg,
                         desc_advance(dy, (set2 ? L::YT : 0) + kg * 2048), id_g, (j > 0 || kg > 0));
           }
-        mma_commit(ds_free(j & 1));
-        mma_commit(y_empty(j % kStages));
+        mma_commit(ds_free(G & 1));
+        mma_commit(y_empty(G % kStages));
       };
+      bool ok = true;
+      int g = 0, ic = 0;
       if (warp == 1) {
-        // T of step st goes in as soon as the softmax warps have loaded T of
-        // step st-1, and runs while they compute dS of step st-1
-        bool ok = wait_bounded(x_full, 0, wc) && wait_bounded(y_full(0), 0, wc);
-        if (ok) {
-          tc_fence_after();
-          issue_t(0);
-          *t_queued = 1;
-        }
-        for (int st = 1; ok && st < n_iter; ++st) {
-          if (!(ok = wait_bounded(y_full(st % kStages), (st / kStages) & 1, wc))) break;
-          if (!(ok = wait_bounded(s_free, (st - 1) & 1, wc))) break;
-          tc_fence_after();
-          issue_t(st);
-          *t_queued = st + 1;
+        // T of step G goes in as soon as the softmax warps have loaded T of
+        // step G-1, and runs while they compute dS of step G-1
+        for (int item = item_first; ok && item < n_items; item += item_stride) {
+          const Item I = item == item_first ? I0 : item_at(item);
+          const int n = item_steps(I);
+          if (n == 0) continue;
+          if (!(ok = wait_bounded(x_full, ic & 1, wc))) break;
+          for (int st = 0; st < n; ++st) {
+            const int G = g + st;
+            if (!(ok = wait_bounded(y_full(G % kStages), (G / kStages) & 1, wc))) break;
+            if (G > 0 && !(ok = wait_bounded(s_free, (G - 1) & 1, wc))) break;
+            tc_fence_after();
+            issue_t(G);
+            *t_queued = G + 1;
+          }
+          if (!ok) break;
+          if (PERSIST) mma_commit(x_free);  // X is read by this item's T GEMMs only
+          g += n;
+          ++ic;
         }
       } else {
-        // gradient GEMMs of step j once its dS is in TMEM, queued behind the T
-        // GEMMs of step j+kGradLag: the next T is on the softmax warps'
-        // critical path, these GEMMs are not (their dS buffer is next written
-        // two steps on). The dQ kernel, bound by the tensor pipe, lags by 2;
-        // the dK kernel, whose shallower Y ring must be released sooner, by 1.
+        // gradient GEMMs of step G once its dS is in TMEM, queued behind the T
+        // GEMMs of step G+kGradLag of the same item: the next T is on the
+        // softmax warps' critical path, these GEMMs are not (their dS buffer is
+        // next written two steps on). The dQ kernel, bound by the tensor pipe,
+        // lags by 2; the dK kernel, whose shallower Y ring must be released
+        // sooner, by 1.
         constexpr int kGradLag = DQ ? 2 : 1;
-        for (int j = 0; j < n_iter; ++j) {
-          if (!wait_bounded(ds_full(j & 1), (j >> 1) & 1, wc)) break;
-          const int need = min(j + kGradLag + 1, n_iter);
-          const uint64_t t0 = global_timer_ns();
-          while (*t_queued < need && !*abort_flag && global_timer_ns() - t0 < timeout_ns) {
+        for (int item = item_first; ok && item < n_items; item += item_stride) {
+          const Item I = item == item_first ? I0 : item_at(item);
+          const int n = item_steps(I);
+          if (n == 0) continue;
+          for (int j = 0; j < n; ++j) {
+            const int G = g + j;
+            if (!(ok = wait_bounded(ds_full(G & 1), (G >> 1) & 1, wc))) break;
+            const int need = min(G + kGradLag + 1, g + n);
+            const uint64_t t0 = global_timer_ns();
+            while (*t_queued < need && !*abort_flag && global_timer_ns() - t0 < timeout_ns) {
+            }
+            // persistent: the previous item's accumulators have been read out
+            if (PERSIST && j == 0 && ic > 0 && !(ok = wait_bounded(acc_empty, (ic - 1) & 1, wc)))
+              break;
+            tc_fence_after();
+            issue_g(G, j);
           }
-          tc_fence_after();
-          issue_g(j);
+          if (!ok) break;
+          mma_commit(acc_full);
+          g += n;
+          ++ic;
         }
-        mma_commit(acc_full);
       }
       mma_commit(drain);
       wait_drain(drain, 0, timeout_ns);
@@ -356,28 +429,33 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     const int grp = (warp - 2) >> 2;   // column group
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // X row within the block = TMEM lane
-    const int xrow = x0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c = scale * kLog2e;
     bool ok = true;
+    int g = 0, ic = 0;
+    for (int item = item_first; ok && item < n_items; item += item_stride) {
+    const Item I = item == item_first ? I0 : item_at(item);
+    const int n_iter = item_steps(I);
+    if (n_iter == 0 && !split_out) continue;
+    const int xrow = I.x0 + r;
 
     // dQ kernel: constants of this thread's query row
     float4 rc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (DQ)
       rc = query_const(lse1_in, lse2_in, g_in, kl_in,
-                       static_cast<size_t>(sv.v_off + static_cast<long long>(xrow) * sv.v_stride),
-                       scale, xrow < nq);
+                       static_cast<size_t>(I.sv.v_off + static_cast<long long>(xrow) * I.sv.v_stride),
+                       scale, xrow < I.nq);
 
-    // T of step `it` into a, b (all lanes agree on every wait's outcome, so
-    // the warp-wide TMEM loads and the __syncwarp below are never reached by
-    // part of a warp); then the T GEMMs of step it+1 may overwrite T
+    // T of global step G into a, b (all lanes agree on every wait's outcome,
+    // so the warp-wide TMEM loads and the __syncwarp below are never reached
+    // by part of a warp); then the T GEMMs of step G+1 may overwrite T
     float a[16], b[16];
-    auto load_t = [&](int it) {
+    auto load_t = [&](int G) {
       // dK kernel: the stage's barrier also publishes its constant table; its
       // phase completed before these T GEMMs were issued, so test it first
       // and let the round trip overlap the T wait
-      const bool tab = DQ || mbar_test_wait(y_full(it % kStages), (it / kStages) & 1);
-      if (!__all_sync(0xffffffffu, wait_bounded(s_full, it & 1, wc))) return false;
+      const bool tab = DQ || mbar_test_wait(y_full(G % kStages), (G / kStages) & 1);
+      if (!__all_sync(0xffffffffu, wait_bounded(s_full, G & 1, wc))) return false;
       tc_fence_after();
       tmem_ld16(tmem + lane_off + L::COL_T + grp * 16, a);
       tmem_ld16(tmem + lane_off + L::COL_T + 64 + grp * 16, b);
@@ -386,34 +464,35 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(s_free);
       return DQ || __all_sync(0xffffffffu, tab) ||
-             __all_sync(0xffffffffu, wait_bounded(y_full(it % kStages), (it / kStages) & 1, wc));
+             __all_sync(0xffffffffu, wait_bounded(y_full(G % kStages), (G / kStages) & 1, wc));
     };
     // The next step's T is loaded right after this step's dS is computed and
     // before it is stored, so the next T GEMMs can start as early as possible.
-    bool good = n_iter > 0 && load_t(0);
+    bool good = n_iter > 0 && load_t(g);
     for (int it = 0; it < n_iter; ++it) {
       if (!good) {
         ok = false;
         break;
       }
-      const int y0 = (y_begin + it) * kStepRows + grp * 16;  // first Y row of this thread's columns
-      // the gradient GEMMs of step it-2 have read this step's dS buffer: nearly
+      const int G = g + it;
+      const int y0 = (I.y_begin + it) * kStepRows + grp * 16;  // first Y row of this thread's columns
+      // the gradient GEMMs of step G-2 have read this step's dS buffer: nearly
       // always done by now; test early, block only if not
-      const bool ds_ready = mbar_test_wait(ds_free(it & 1), ((it >> 1) & 1) ^ 1);
+      const bool ds_ready = mbar_test_wait(ds_free(G & 1), ((G >> 1) & 1) ^ 1);
       uint32_t d2p[8], d1p[8];
       {
         // visibility of (query, key) over this thread's 16 columns
         bool full;
         int lim = 0;
         if (DQ) {
-          lim = causal ? min(nk, xrow + 1 + off) : nk;  // keys < lim visible
+          lim = causal ? min(I.nk, xrow + 1 + I.off) : I.nk;  // keys < lim visible
           full = y0 + 16 <= lim;
         } else {
-          lim = causal ? xrow - off : 0;  // queries >= lim (and < N_Q) see this key
-          full = y0 + 16 <= nq && y0 >= lim;
+          lim = causal ? xrow - I.off : 0;  // queries >= lim (and < N_Q) see this key
+          full = y0 + 16 <= I.nq && y0 >= lim;
         }
-        auto visible = [&](int y) { return DQ ? y < lim : (y < nq && y >= lim); };
-        const float* tq = tab + (it % kStages) * 4 * kStepRows + grp * 16;
+        auto visible = [&](int y) { return DQ ? y < lim : (y < I.nq && y >= lim); };
+        const float* tq = tab + (G % kStages) * 4 * kStepRows + grp * 16;
         const float2 c2 = make_float2(c, c), sc2 = make_float2(scale, scale);
         const float2 m1 = make_float2(-1.f, -1.f);
         float4 q1c, q2c, qgc, qec;  // dK kernel: 4 columns of each constant, one 16-byte load each
@@ -461,22 +540,22 @@ __global__ void __launch_bounds__(kSepThreads, 1)
           }
         }
       }
-      if (it + 1 < n_iter) good = load_t(it + 1);
+      if (it + 1 < n_iter) good = load_t(G + 1);
       if (!__all_sync(0xffffffffu, ds_ready) &&
-          !__all_sync(0xffffffffu, wait_bounded(ds_free(it & 1), ((it >> 1) & 1) ^ 1, wc))) {
+          !__all_sync(0xffffffffu, wait_bounded(ds_free(G & 1), ((G >> 1) & 1) ^ 1, wc))) {
         ok = false;
         break;
       }
       // this thread's 16 values of row r: 8 packed columns per set at
-      // [8 grp, 8 grp + 8) of the set's 32-column slot of buffer it&1
-      const uint32_t dsb = tmem + lane_off + L::COL_DS + (it & 1) * 64 + grp * 8;
+      // [8 grp, 8 grp + 8) of the set's 32-column slot of buffer G&1
+      const uint32_t dsb = tmem + lane_off + L::COL_DS + (G & 1) * 64 + grp * 8;
       tc_fence_after();  // the stores below follow the MMAs that read this buffer
       if (HAS2) tmem_st8(dsb, d2p);
       if (HAS1) tmem_st8(dsb + (HAS2 ? 32 : 0), d1p);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full(it & 1));
+      if (lane == 0) mbar_arrive(ds_full(G & 1));
     }
     // epilogue: accumulator row r -> bf16 dQ (dQ kernel) or dK (dK kernel)
     // row, d columns [grp d/4, (grp+1) d/4); with a key split, the fp32 row
@@ -487,9 +566,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       const size_t plane = static_cast<size_t>(gridDim.y) * NQ;
       return reinterpret_cast<float4*>(
           part + ((static_cast<size_t>(t) * splits + blockIdx.z) * plane +
-                  static_cast<size_t>(sv.v_off + xrow)) * D + grp * EC);
+                  static_cast<size_t>(I.sv.v_off + xrow)) * D + grp * EC);
     };
-    if (split_out && ok && active && n_iter == 0 && xrow < NX) {
+    if (split_out && ok && I.active && n_iter == 0 && xrow < I.NX) {
 #pragma unroll
       for (int t = 0; t < L::NSETS; ++t) {
         float4* dst = part_row(t);
@@ -497,7 +576,7 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         for (int i = 0; i < EC / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    if (ok && n_iter > 0 && __all_sync(0xffffffffu, wait_bounded(acc_full, 0, wc))) {
+    if (ok && n_iter > 0 && __all_sync(0xffffffffu, wait_bounded(acc_full, ic & 1, wc))) {
       tc_fence_after();
 #pragma unroll
       for (int t = 0; t < L::NSETS; ++t) {
@@ -508,7 +587,7 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         else
           tmem_ld16(tmem + lane_off + L::COL_ACC + t * D + grp * EC, v);
         tmem_wait_ld();
-        if (xrow < NX) {
+        if (xrow < I.NX) {
           if (split_out) {
             float4* dst = part_row(t);
 #pragma unroll
@@ -516,7 +595,7 @@ __global__ void __launch_bounds__(kSepThreads, 1)
               dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
           } else {
             uint4* dst = reinterpret_cast<uint4*>(
-                out + (DQ ? sv.q_off : sv.k_off) + static_cast<long long>(xrow) * sv.row_stride +
+                out + (DQ ? I.sv.q_off : I.sv.k_off) + static_cast<long long>(xrow) * I.sv.row_stride +
                 grp * EC);
 #pragma unroll
             for (int i = 0; i < EC / 8; ++i)
@@ -527,6 +606,16 @@ __global__ void __launch_bounds__(kSepThreads, 1)
           }
         }
       }
+      if (PERSIST) {  // the next item's gradient GEMMs may overwrite the accumulators
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+      }
+    } else {
+      ok = false;
+    }
+    g += n_iter;
+    ++ic;
     }
   }
 
@@ -563,15 +652,16 @@ __global__ void streamkl_dq_split_combine_kernel(const float* __restrict__ part,
                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
 }
 
-template <int D, bool DQ, int SETS, bool PACKED>
+template <int D, bool DQ, int SETS, bool PACKED, bool PERSIST>
 cudaError_t launch_sep_p(const BwdSepArgs& a, cudaStream_t stream) {
   using L = SepLayout<D, DQ, SETS>;
-  auto kern = streamkl_bwd_sep_kernel<D, DQ, SETS, PACKED>;
+  auto kern = streamkl_bwd_sep_kernel<D, DQ, SETS, PACKED, PERSIST>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
   if (e != cudaSuccess) return e;
   const int NX = DQ ? a.NQ : a.NK;  // the longest sequence for packed batches
   const int splits = (DQ && !PACKED) ? a.dq_splits : 1;
   dim3 grid((NX + kBlockM - 1) / kBlockM, a.BH, splits);
+  if (PERSIST) grid = dim3(a.dk_persist_ctas, 1, 1);
   const CUtensorMap* x1 = DQ ? a.tm_q1 : a.tm_k1;
   const CUtensorMap* x2 = DQ ? a.tm_q2 : a.tm_k2;
   const CUtensorMap* y1 = DQ ? a.tm_k1 : a.tm_q1;
@@ -580,14 +670,16 @@ cudaError_t launch_sep_p(const BwdSepArgs& a, cudaStream_t stream) {
       *x1, *x2, *y1, *y2, a.NQ, a.NK, a.causal, a.scale, a.kl, a.lse1, a.lse2, a.g,
       static_cast<__nv_bfloat16*>(DQ ? a.dq2 : a.dk2),
       static_cast<__nv_bfloat16*>(DQ ? a.dq1 : a.dk1), splits > 1 ? a.dq_part : nullptr, splits,
-      a.dq_split_steps, a.cu_q, a.cu_k, a.H, a.total_q, a.total_k, a.dev_status, a.timeout_ns);
+      a.dq_split_steps, a.BH, a.cu_q, a.cu_k, a.H, a.total_q, a.total_k, a.dev_status,
+      a.timeout_ns);
   return cudaGetLastError();
 }
 
 template <int D, bool DQ, int SETS>
 cudaError_t launch_sep_t(const BwdSepArgs& a, cudaStream_t stream) {
-  return a.cu_q != nullptr ? launch_sep_p<D, DQ, SETS, true>(a, stream)
-                           : launch_sep_p<D, DQ, SETS, false>(a, stream);
+  if (a.cu_q != nullptr) return launch_sep_p<D, DQ, SETS, true, false>(a, stream);
+  if (!DQ && a.dk_persist_ctas > 0) return launch_sep_p<D, DQ, SETS, false, !DQ>(a, stream);
+  return launch_sep_p<D, DQ, SETS, false, false>(a, stream);
 }
 
 template <int D, bool DQ>

@@ -130,6 +130,9 @@ struct BwdSepArgs {
   // into chunks of dq_split_steps; partial dQ rows go to dq_part (fp32
   // [sets][dq_splits][BH NQ][d]) and a combine kernel sums them
   int dq_splits = 1, dq_split_steps = 0;
+  // dK kernel as a persistent grid of this many CTAs over (key block, batch-head)
+  // items (dense batches; 0: one CTA per key block)
+  int dk_persist_ctas = 0;
   float* dq_part = nullptr;
   int* dev_status;
   uint64_t timeout_ns;

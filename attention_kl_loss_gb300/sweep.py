@@ -5,6 +5,7 @@
     python -m attention_kl_loss_gb300.sweep context   # context length 4K .. 512K
     python -m attention_kl_loss_gb300.sweep dqsplit   # backward dQ key split on/off
     python -m attention_kl_loss_gb300.sweep configs   # the named workloads, fwd and bwd
+    python -m attention_kl_loss_gb300.sweep dkpersist # persistent dK kernel off/on, short queries
 
 Every point is timed through the C ABI with CUDA events on the current stream,
 inputs resident in device memory, one untimed call first, the median of
@@ -138,6 +139,38 @@ def sweep_dqsplit(reps: int):
         torch.cuda.empty_cache()
 
 
+def sweep_dkpersist(reps: int):
+    """Separate backward with the persistent dK kernel off and at the
+    library's choice, for short query sweeps against long keys."""
+    dev = torch.device("cuda")
+    shapes = [synthetic.custom(f"q{nq}_k64k_b4h32", B=4, H=32, NQ=nq, NK=65536, d=128, causal=True,
+                               noise=0.1) for nq in (64, 128, 256, 384, 512, 1024)] + [
+        synthetic.custom("q128_k128k_b1h32", B=1, H=32, NQ=128, NK=131072, d=128, causal=True,
+                         noise=0.1, grad1=True),
+        synthetic.WORKLOADS["splitk"]]
+    print("| workload | sets | persistent CTAs chosen | ms, off | ms, chosen | speed-up |")
+    print("|---|---|---:|---:|---:|---:|")
+    for w in shapes:
+        (q1, k1, q2, k2, g), st = _setup(w, dev)
+        kl, l1, l2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, dev_status=st)
+        res = {}
+        for forced in (-1, None):
+            binding.set_bwd_dk_persist(forced)
+            try:
+                res[forced] = _time(lambda: binding.streamkl_bwd(
+                    q1, k1, q2, k2, kl, l1, l2, g, w.scale, w.causal, grad1=w.grad1,
+                    dev_status=st), reps)
+            finally:
+                binding.set_bwd_dk_persist(None)
+        _check(st, w.name)
+        c = binding.bwd_dk_persist(w.B, w.H, w.NQ, w.NK, w.d, w.causal)
+        print(f"| {w.name} (B{w.B} H{w.H} {w.NQ}x{w.NK} d{w.d} causal) | "
+              f"{'both' if w.grad1 else 'config 1'} | {c} | {res[-1]:.3f} | {res[None]:.3f} | "
+              f"{res[-1] / res[None]:.2f} |")
+        del q1, k1, q2, k2, g
+        torch.cuda.empty_cache()
+
+
 def sweep_configs(reps: int):
     """Forward and backward of every named workload at the library's choices,
     with the exact visible-pair FLOP counts: 4d per pair forward; the
@@ -210,12 +243,12 @@ def sweep_context(reps: int):
 
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    p.add_argument("what", choices=["algo", "decode", "context", "dqsplit", "configs"])
+    p.add_argument("what", choices=["algo", "decode", "context", "dqsplit", "configs", "dkpersist"])
     p.add_argument("--reps", type=int, default=3)
     a = p.parse_args(argv)
     binding.load()
     {"algo": sweep_algo, "decode": sweep_decode, "context": sweep_context,
-     "dqsplit": sweep_dqsplit, "configs": sweep_configs}[a.what](a.reps)
+     "dqsplit": sweep_dqsplit, "configs": sweep_configs, "dkpersist": sweep_dkpersist}[a.what](a.reps)
 
 
 if __name__ == "__main__":

@@ -114,6 +114,22 @@ int streamkl_bwd_dq_splits(int B, int H, int NQ, int NK, int d, int causal, int 
 int streamkl_set_bwd_dq_splits(int splits);
 
 /*
+ * Persistent dK kernel of the separate algorithm for short query sweeps
+ * (N_Q <= 512, dense batches, more (key block, batch-head) items than SMs):
+ * one CTA per SM takes the items in turn, heavy key blocks first, and loads
+ * the next item's key block while the current one finishes, instead of one
+ * CTA per key block paying its start and end each time. No counterpart in
+ * the paper; same results.
+ *   streamkl_bwd_dk_persist: the number of persistent CTAs streamkl_bwd will
+ *        launch for these sizes (0: one CTA per key block); -1 on invalid sizes.
+ *   streamkl_set_bwd_dk_persist: process-wide override, 0 = automatic,
+ *        -1 = never, n >= 1 = always, with n CTAs; same threading caveat as
+ *        streamkl_set_bwd_algorithm. Returns 0, or -1 below -1.
+ */
+int streamkl_bwd_dk_persist(int B, int H, int NQ, int NK, int d, int causal);
+int streamkl_set_bwd_dk_persist(int ctas);
+
+/*
  * Workspace bytes the backward pass needs, for one gradient set or, with
  * want_grad1 != 0, both (an upper bound for configuration 2 alone): for the
  * separate-kernel algorithm the fp32 partials of the dQ kernel's key split

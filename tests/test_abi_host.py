@@ -118,6 +118,28 @@ def test_dq_key_split_choice(lib):
         lib.streamkl_set_bwd_dq_splits(0)
 
 
+def test_persistent_dk_choice(lib):
+    """The persistent dK kernel is used for short query sweeps (N_Q <= 512)
+    with more (key block, batch-head) items than SMs, one CTA per SM; the
+    override forces or disables it."""
+    lib.streamkl_set_bwd_dk_persist(0)
+    sms = lib.streamkl_bwd_dk_persist(4, 32, 512, 131072, 128, 1)
+    assert sms > 0  # 1024 key blocks x 128 slices
+    assert lib.streamkl_bwd_dk_persist(4, 32, 64, 65536, 128, 1) == sms
+    assert lib.streamkl_bwd_dk_persist(4, 32, 1024, 65536, 128, 1) == 0
+    assert lib.streamkl_bwd_dk_persist(1, 32, 65536, 65536, 128, 1) == 0
+    assert lib.streamkl_bwd_dk_persist(1, 1, 512, 512, 64, 0) == 0  # 4 items: fewer than SMs
+    assert lib.streamkl_bwd_dk_persist(1, 1, 8, 4, 64, 1) == -1  # invalid sizes
+    try:
+        assert lib.streamkl_set_bwd_dk_persist(3) == 0
+        assert lib.streamkl_bwd_dk_persist(1, 32, 65536, 65536, 128, 1) == 3
+        assert lib.streamkl_set_bwd_dk_persist(-1) == 0
+        assert lib.streamkl_bwd_dk_persist(4, 32, 512, 131072, 128, 1) == 0
+        assert lib.streamkl_set_bwd_dk_persist(-2) == -1
+    finally:
+        lib.streamkl_set_bwd_dk_persist(0)
+
+
 def test_forced_split_workspace_rounding(lib):
     # 100 rows, 2 key tiles, request 16 splits -> 2 effective splits
     n = 5 * 2 * 1 * 100 * 4

@@ -230,6 +230,52 @@ def test_dq_key_split(NQ, NK, d, causal, sets, splits):
             assert_grad(host(grads[i][0, hh]), og[i], name)
 
 
+@pytest.mark.parametrize("ctas", [1, 3, 7])
+@pytest.mark.parametrize("NQ,NK,d,causal,sets", [
+    (200, 2000, 128, True, "both"),
+    (130, 1500, 64, False, "config1"),
+    (640, 700, 128, True, "config2"),
+    (64, 4096, 128, True, "config1"),  # one query step per key block
+])
+def test_persistent_dk_kernel(NQ, NK, d, causal, sets, ctas):
+    """The dK kernel as a persistent grid of `ctas` CTAs, each taking many
+    (key block, batch-head) items in turn: dK bit-identical to one CTA per
+    key block (same arithmetic per item) and equal to the oracle."""
+    w = synthetic.custom(f"persist_{NQ}x{NK}d{d}", B=2, H=2, NQ=NQ, NK=NK, d=d, causal=causal,
+                         noise=0.5, grad1=sets != "config1")
+    dev = torch.device("cuda")
+    ins = synthetic.make_inputs(w, 17, dev)
+    q1, k1, q2, k2, g = ins
+    status = binding.new_status(dev)
+    kl, lse1, lse2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, dev_status=status)
+    g1, g2 = sets != "config1", sets != "config2"
+    binding.set_bwd_algorithm(binding.BWD_SEPARATE)
+    try:
+        binding.set_bwd_dk_persist(-1)
+        ref = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                   grad1=g1, grad2=g2, dev_status=status)
+        binding.set_bwd_dk_persist(ctas)
+        assert binding.bwd_dk_persist(w.B, w.H, NQ, NK, d, causal) == ctas
+        got = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                   grad1=g1, grad2=g2, dev_status=status)
+    finally:
+        binding.set_bwd_dk_persist(None)
+        binding.set_bwd_algorithm(None)
+    binding.raise_on_device_status(status, "persistent dK kernel")
+    for i in range(4):
+        assert (got[i] is None) == (ref[i] is None)
+        if got[i] is not None:
+            assert torch.equal(got[i], ref[i]), ["dq2", "dk2", "dq1", "dk1"][i]
+    for b in range(w.B):
+        for hh in range(w.H):
+            h = [host(t[b, hh]) for t in ins[:4]]
+            og = orc.head_backward(*h, w.scale, w.causal, g[b, hh].cpu().numpy().astype(np.float64),
+                                   True)
+            for i, name in enumerate(["dq2", "dk2", "dq1", "dk1"]):
+                if got[i] is not None:
+                    assert_grad(host(got[i][b, hh]), og[i], name)
+
+
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("NQ,NK,d,causal", [(256, 256, 64, False), (200, 333, 128, True)])
 def test_reverse_direction(NQ, NK, d, causal, algo):
