@@ -77,8 +77,8 @@ struct SepLayout {
   static constexpr int TAB_BYTES = DQ ? 0 : STAGES * 4 * kStepRows * 4;
   static constexpr int OFF_BAR = OFF_TAB + TAB_BYTES;
   // x_full, y_full[S], y_empty[S], s_full, s_free, ds_full[2], ds_free[2],
-  // acc_full, drain
-  static constexpr int NBAR = 1 + 2 * STAGES + 8;
+  // acc_full, drain, x_free, acc_empty (the last two: persistent kernel)
+  static constexpr int NBAR = 1 + 2 * STAGES + 10;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;
@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   // persistent: X of the next item may be loaded; the accumulators were read
   const uint32_t x_free = s_full + 64;
   const uint32_t acc_empty = s_full + 72;
+  static_assert(1 + 2 * kStages + 10 <= L::NBAR, "barrier region holds every barrier");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
   volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
