@@ -276,6 +276,37 @@ def test_persistent_dk_kernel(NQ, NK, d, causal, sets, ctas):
                     assert_grad(host(got[i][b, hh]), og[i], name)
 
 
+def test_decode_shape_automatic_paths():
+    """A decode-like shape (64 query rows against 8K keys, 4 slices) with both
+    gradient sets through the reverse entry points and the library's own
+    choices, which here are the persistent dK kernel and a dQ key split;
+    against the oracle's definition with the distributions in that order."""
+    w = synthetic.custom("decode_auto", B=2, H=2, NQ=64, NK=8192, d=128, causal=True, noise=0.4,
+                         grad1=True)
+    assert binding.bwd_dk_persist(w.B, w.H, w.NQ, w.NK, w.d, w.causal) > 0
+    assert binding.bwd_dq_splits(w.B, w.H, w.NQ, w.NK, w.d, w.causal, True) > 1
+    dev = torch.device("cuda")
+    ins = synthetic.make_inputs(w, 23, dev)
+    q1, k1, q2, k2, g = ins
+    status = binding.new_status(dev)
+    kl, lse1, lse2 = binding.streamkl_fwd_reverse(q1, k1, q2, k2, w.scale, w.causal,
+                                                  dev_status=status)
+    grads = binding.streamkl_bwd_reverse(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                         grad1=True, dev_status=status)
+    binding.raise_on_device_status(status, "decode shape")
+    for b in range(w.B):
+        for hh in range(w.H):
+            h1q, h1k, h2q, h2k = (host(t[b, hh]) for t in ins[:4])
+            rkl, _, _ = orc.head_forward(h2q, h2k, h1q, h1k, w.scale, w.causal)
+            assert_kl(host(kl[b, hh]), rkl)
+            t_dq, t_dk, s_dq, s_dk = orc.head_backward(h2q, h2k, h1q, h1k, w.scale, w.causal,
+                                                       g[b, hh].cpu().numpy().astype(np.float64),
+                                                       True)
+            for got, ref, name in ((grads[0], s_dq, "student dq2"), (grads[1], s_dk, "student dk2"),
+                                   (grads[2], t_dq, "teacher dq1"), (grads[3], t_dk, "teacher dk1")):
+                assert_grad(host(got[b, hh]), ref, name)
+
+
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("NQ,NK,d,causal", [(256, 256, 64, False), (200, 333, 128, True)])
 def test_reverse_direction(NQ, NK, d, causal, algo):
