@@ -486,25 +486,59 @@ namespace {
 constexpr size_t kFwdScratchBytes = size_t(16) << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_fwd_scratch[kFwdScratchBytes];
 
+// Device address of g_fwd_scratch, per device, and the driver context it was
+// looked up in. The library's module (and with it the array) is loaded anew
+// in every context: after cudaDeviceReset, or while the caller has another
+// driver context current, the array lives at another address.
+struct ScratchAddr {
+  CUcontext ctx;
+  void* ptr;
+};
 std::mutex g_scratch_mu;
-void* g_scratch_dev_ptr[256] = {};  // device address of g_fwd_scratch, per device
+ScratchAddr g_scratch_addr[256] = {};
 
-// Device address of the scratch array on the current device. The host-side
-// name of the array is only a stand-in, so the address is looked up once per
-// device (with that device current) and cached.
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+std::once_flag g_ctx_current_once;
+
+PFN_cuCtxGetCurrent_v4000 ctx_current_fn() {
+  std::call_once(g_ctx_current_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+  });
+  return g_ctx_current;
+}
+
+// Device address of the scratch array in the current device's current
+// context. The host-side name of the array is only a stand-in, so the address
+// is looked up with that device current, cached, and looked up again whenever
+// the current context differs from the one the cached address came from.
 streamkl_status fwd_scratch_ptr(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 256) return fail(STREAMKL_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  auto get_ctx = ctx_current_fn();
+  if (!get_ctx) return fail(STREAMKL_ERR_CUDA, "cuCtxGetCurrent unavailable from the driver");
+  CUcontext ctx = nullptr;
+  if (get_ctx(&ctx) != CUDA_SUCCESS) return fail(STREAMKL_ERR_CUDA, "cuCtxGetCurrent failed");
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_dev_ptr[dev]) {
+  ScratchAddr& c = g_scratch_addr[dev];
+  if (!c.ptr || ctx == nullptr || c.ctx != ctx) {
     void* p = nullptr;
+    // a runtime call: it also creates the device's primary context when no
+    // context is current yet, so the context is read again afterwards
     e = cudaGetSymbolAddress(&p, g_fwd_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
-    g_scratch_dev_ptr[dev] = p;
+    if (get_ctx(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+      return fail(STREAMKL_ERR_CUDA, "no current CUDA context");
+    c.ctx = ctx;
+    c.ptr = p;
   }
-  *out = g_scratch_dev_ptr[dev];
+  *out = c.ptr;
   return STREAMKL_OK;
 }
 

@@ -10,9 +10,18 @@ Metric: fwd+bwd TFLOP/s at that workload with the usual attention convention,
 The value is device-timed with inputs resident in HBM (inputs are 2 GiB, far
 larger than the 129 MB L2, so no flush is needed between steps). ``e2e`` is
 the same metric through the public Python API with host (pinned) buffers:
-each step copies the inputs in and the per-row KL out (the batch streamed in
-groups of heads: a group's copy runs on a second stream while the previous
-group computes).
+each step copies the inputs in and every result out (KL, LSE1, LSE2 and the
+four gradients), the batch streamed in groups of heads: a group's inputs are
+copied in on one stream and the previous group's results out on another
+while the group in between computes.
+
+``roofline`` counts the method's work: 4d FLOPs per visible (query, key) pair
+for the forward, and for the backward 4d to regenerate S1, S2 plus 4d per
+gradient set (12d with both sets); what the kernels execute (the separate
+dK and dQ kernels each regenerate S1 and S2: 16d) is reported beside it.
+``configs`` holds one entry per named workload (times, the same counts, and
+the GPU results' error against the oracle on the sample the CPU-baseline leg
+times).
 
 ``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
 bounded sample of the same workload per step).
@@ -53,6 +62,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=15.0,
                    help="target CPU seconds for the oracle sample")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the per-workload entries (times and oracle errors)")
     return p.parse_args(argv)
 
 
@@ -97,15 +108,39 @@ def replica_seed(rank: int) -> int:
 
 # --------------------------------------------------------------------------- work counts
 def flop_counts(w):
-    """(fwd, bwd_metric, bwd_work, fwd_exact, bwd_work_exact) FLOPs for one step."""
-    bh = w.B * w.H
-    dense = w.NQ * w.NK * w.d * bh
+    """(fwd, bwd_metric) FLOPs for one step in the headline convention:
+    4 N_Q N_K d forward and 8 N_Q N_K d backward per head, halved for causal."""
+    dense = w.NQ * w.NK * w.d * w.B * w.H
     half = 0.5 if w.causal else 1.0
-    pairs = w.live_pairs_per_head() * bh
-    fwd = 4 * dense * half
-    bwd_metric = 8 * dense * half
-    g = 12 if w.grad1 else 8
-    return fwd, bwd_metric, g * dense * half, 4 * pairs * w.d, g * pairs * w.d
+    return 4 * dense * half, 8 * dense * half
+
+
+def method_flops(w):
+    """(fwd, bwd) FLOPs of the method's work on the exact visible pairs: the
+    forward's two score GEMMs (4d per pair); the backward's regeneration of
+    S1, S2 (4d) plus dQ_t and dK_t (4d) per gradient set."""
+    pairs = w.live_pairs_per_head() * w.B * w.H
+    sets = 2 if w.grad1 else 1
+    return 4 * pairs * w.d, (4 + 4 * sets) * pairs * w.d
+
+
+def executed_bwd_flops(w, separate: bool):
+    """Backward FLOPs the kernels execute: the separate dK and dQ kernels each
+    regenerate S1 and S2, the fused kernel once."""
+    pairs = w.live_pairs_per_head() * w.B * w.H
+    sets = 2 if w.grad1 else 1
+    return ((8 if separate else 4) + 4 * sets) * pairs * w.d
+
+
+def bwd_min_bytes(w):
+    """Bytes the backward must move at least: the four inputs once, the
+    gradients it writes once, and the per-row vectors it reads (KL, LSE1,
+    LSE2, g)."""
+    bh = w.B * w.H
+    q = bh * w.NQ * w.d * 2
+    k = bh * w.NK * w.d * 2
+    sets = 2 if w.grad1 else 1
+    return 2 * (q + k) + sets * (q + k) + 4 * bh * w.NQ * 4
 
 
 def peaks():
@@ -182,13 +217,11 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- CPU oracle
-def oracle_sample(w, budget_s: float, seed: int = 7):
-    """Time the fp64 oracle (fwd + bwd, both gradient sets) on the last R query
-    rows of one head, growing R until the sample takes ~budget_s seconds.
-    Returns (tflops, seconds, flops, description)."""
+def draw_head(w, seed: int = 7):
+    """One (batch, head) slice of the workload's recipe drawn on the host
+    (numpy, rounded to bf16), for the reference arm, which has no GPU inputs:
+    (q1, k1, q2, k2, g) as fp64 arrays."""
     import numpy as np
-    from oracle import streamkl_oracle as orc
-
     rng = np.random.default_rng(seed)
 
     def bf16(x):
@@ -202,22 +235,42 @@ def oracle_sample(w, budget_s: float, seed: int = 7):
     q2 = bf16(q1 + w.noise * rng.standard_normal((w.NQ, w.d)))
     k2 = bf16(k1 + w.noise * rng.standard_normal((w.NK, w.d)))
     g = np.full(w.NQ, 1.0 / (w.B * w.H * w.NQ))
+    return q1, k1, q2, k2, g
+
+
+def oracle_rows(w, head, rows):
+    """The fp64 oracle (forward + backward with the workload's gradient sets)
+    on query rows `rows` of one head given as host arrays. Returns
+    (seconds, visible pairs, (kl, lse1, lse2), (dq2, dk2, dq1, dk1))."""
+    import numpy as np
+    from oracle import streamkl_oracle as orc
+    q1, k1, q2, k2, g = head
+    t0 = time.perf_counter()
+    fwd = orc.head_forward(q1, k1, q2, k2, w.scale, w.causal, rows=rows)
+    bwd = orc.head_backward(q1, k1, q2, k2, w.scale, w.causal, g, w.grad1, rows=rows)
+    dt = time.perf_counter() - t0
     off = w.NK - w.NQ
+    pairs = int(np.sum(np.minimum(w.NK, rows + 1 + off))) if w.causal else len(rows) * w.NK
+    return dt, pairs, fwd, bwd
+
+
+def oracle_sample(w, budget_s: float, head):
+    """Time the oracle on the last R query rows of one head, doubling R until
+    the sample takes about budget_s / 3 seconds. Returns (TFLOP/s in the
+    metric's convention on the sample's visible pairs, seconds, rows, oracle
+    outputs, description)."""
+    import numpy as np
     r = 64
     while True:
         rows = np.arange(w.NQ - r, w.NQ)
-        t0 = time.perf_counter()
-        orc.head_forward(q1, k1, q2, k2, w.scale, w.causal, rows=rows)
-        orc.head_backward(q1, k1, q2, k2, w.scale, w.causal, g, w.grad1, rows=rows)
-        dt = time.perf_counter() - t0
-        pairs = int(np.sum(np.minimum(w.NK, rows + 1 + off))) if w.causal else r * w.NK
+        dt, pairs, fwd, bwd = oracle_rows(w, head, rows)
         # metric convention on the exact pairs of the sample: (4 + 8) d per pair
         flops = 12.0 * pairs * w.d
         if dt >= budget_s / 3 or r >= w.NQ:
-            desc = (f"head 0 of a fresh draw, last {r} query rows (all their {pairs} visible "
-                    f"(query,key) pairs), forward + backward"
+            desc = (f"last {r} query rows of one head (all their {pairs} visible (query,key) "
+                    f"pairs), forward + backward"
                     f"{' with both gradient sets' if w.grad1 else ''}, fp64 numpy")
-            return flops / dt / 1e12, dt, flops, desc
+            return flops / dt / 1e12, dt, rows, (fwd, bwd), desc
         r = min(w.NQ, r * 2)
 
 
@@ -232,6 +285,54 @@ def cpu_cores():
     return os.cpu_count() or 1
 
 
+def _rel_l2(got, ref):
+    import numpy as np
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+def error_stats(w, rows, oracle_out, gpu_head):
+    """The GPU results of one head against the oracle's on `rows`: KL as the
+    largest |error| / (2e-3 + 1e-2 |ref|) (pass <= 1), relative L2 of LSE1,
+    LSE2 and of each gradient (pass <= 1e-4 and 1e-2). dK is compared on the
+    keys that only `rows` see (all keys when rows are all rows; the last
+    len(rows) keys under the causal mask), where a row sample gives it
+    exactly."""
+    import numpy as np
+    (okl, ol1, ol2), og = oracle_out
+    kl, l1, l2, grads = gpu_head
+    err = np.abs(kl[rows] - okl)
+    st = {"kl_max_err_over_bound": float(np.max(err / (2e-3 + 1e-2 * np.abs(okl)))),
+          "lse1_rel_l2": _rel_l2(l1[rows], ol1), "lse2_rel_l2": _rel_l2(l2[rows], ol2)}
+    if len(rows) == w.NQ:
+        keys = np.arange(w.NK)
+    elif w.causal:
+        keys = np.arange(w.NK - len(rows), w.NK)
+    else:
+        keys = None
+    names = ["dq2", "dk2", "dq1", "dk1"]
+    for i, name in enumerate(names):
+        if grads[i] is None or og[i] is None:
+            continue
+        if name.startswith("dq"):
+            st[f"{name}_rel_l2"] = _rel_l2(grads[i][rows], og[i])
+        elif keys is not None:
+            st[f"{name}_rel_l2"] = _rel_l2(grads[i][keys], og[i][keys])
+    st["dk_keys_compared"] = 0 if keys is None else int(len(keys))
+    st["pass"] = bool(st["kl_max_err_over_bound"] <= 1.0 and st["lse1_rel_l2"] <= 1e-4
+                      and st["lse2_rel_l2"] <= 1e-4
+                      and all(v <= 1e-2 for k, v in st.items() if k.startswith("d")
+                              and k.endswith("_rel_l2")))
+    return st
+
+
+def host_head(tensors, b, h):
+    """fp64 host copies of slice (b, h) of device tensors (None stays None)."""
+    return [None if t is None else t[b, h].float().cpu().numpy().astype("float64")
+            for t in tensors]
+
+
 # --------------------------------------------------------------------------- arms
 def emit(obj):
     print(json.dumps(obj), flush=True)
@@ -242,12 +343,13 @@ def reference_arm(args, w):
     if rank != 0:
         return 0
     budget = args.cpu_budget_s
+    head = draw_head(w)
     for _ in range(args.warmup):
-        oracle_sample(w, min(budget, 2.0))
+        oracle_sample(w, min(budget, 2.0), head)
     vals, times = [], []
     desc = ""
     for _ in range(args.steps):
-        v, dt, flops, desc = oracle_sample(w, budget / max(1, args.steps))
+        v, dt, _, _, desc = oracle_sample(w, budget / max(1, args.steps), head)
         vals.append(v)
         times.append(dt)
     value = statistics.median(vals)
@@ -258,7 +360,7 @@ def reference_arm(args, w):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": describe(w)},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": desc},
+                         "sample": f"head 0 of a host draw of the recipe, {desc}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     })
@@ -293,6 +395,85 @@ def describe(w):
     return (f"{w.name}: B={w.B} H={w.H} N_Q={w.NQ} N_K={w.NK} d={w.d} "
             f"{'causal' if w.causal else 'non-causal'}, bf16 inputs, fwd+bwd"
             f"{' incl. dQ1,dK1' if w.grad1 else ''}")
+
+
+def _time_calls(fn, reps, stream):
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    out = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        out.append(a.elapsed_time(b))
+    return statistics.median(out)
+
+
+# Oracle sample per named workload in the per-config entries: which head and
+# how many of its last query rows (None: all rows; all heads for "tiny").
+CONFIG_SAMPLES = {"tiny": None, "mid": ((1, 15), None), "splitk": ((3, 31), None),
+                  "stress": ((0, 7), 1024)}
+
+
+def config_entry(w, binding, synthetic, dev, pk, seed):
+    """One named workload at full size: forward and backward times (median of
+    3 timed calls after one untimed, CUDA events, inputs resident), method
+    and executed TFLOP/s, and the error against the oracle on a sample."""
+    import numpy as np
+    import torch
+    q1, k1, q2, k2, g = synthetic.make_inputs(w, seed, dev)
+    B, H, NQ, NK, d = w.B, w.H, w.NQ, w.NK, w.d
+    ws_bytes = binding.streamkl_workspace_size(B, H, NQ, NK, d, w.causal, w.grad1)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    status = binding.new_status(dev)
+    outs = tuple(torch.empty((B, H, NQ), dtype=torch.float32, device=dev) for _ in range(3))
+    grads = (torch.empty_like(q2), torch.empty_like(k2),
+             torch.empty_like(q1) if w.grad1 else None, torch.empty_like(k1) if w.grad1 else None)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, out=outs, workspace=ws,
+                             dev_status=status)
+
+    def bwd():
+        binding.streamkl_bwd(q1, k1, q2, k2, *outs, g, w.scale, w.causal, grad1=w.grad1, out=grads,
+                             workspace=ws, dev_status=status)
+
+    fwd_ms = _time_calls(fwd, 3, stream)
+    bwd_ms = _time_calls(bwd, 3, stream)
+    binding.raise_on_device_status(status, w.name)
+    separate = binding.bwd_algorithm(B, H, NQ, NK, d, w.causal, w.grad1) == binding.BWD_SEPARATE
+    mf, mb = method_flops(w)
+    xb = executed_bwd_flops(w, separate)
+    sus = pk["bf16_tflops_sustained"]
+    e = {"workload": describe(w), "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+         "fwd_tflops": mf / fwd_ms / 1e9, "bwd_tflops_method": mb / bwd_ms / 1e9,
+         "bwd_tflops_executed": xb / bwd_ms / 1e9,
+         "frac_of_measured_sustained": {"fwd": mf / fwd_ms / 1e9 / sus,
+                                        "bwd_method": mb / bwd_ms / 1e9 / sus}}
+    # the oracle on a sample of the same inputs (the CPU-baseline leg's work)
+    plan = CONFIG_SAMPLES.get(w.name)
+    heads = [(b, h) for b in range(B) for h in range(H)] if plan is None else [plan[0]]
+    r = None if plan is None else plan[1]
+    stats, secs = [], 0.0
+    for (b, h) in heads:
+        head = host_head((q1, k1, q2, k2, g), b, h)
+        rows = np.arange(NQ) if r is None else np.arange(NQ - r, NQ)
+        dt, _, fo, bo = oracle_rows(w, head, rows)
+        secs += dt
+        gpu = host_head(outs + grads, b, h)
+        stats.append(error_stats(w, rows, (fo, bo), (gpu[0], gpu[1], gpu[2], gpu[3:])))
+    worst = {k: max(s[k] for s in stats) for k in stats[0] if k not in ("pass",)}
+    worst["pass"] = all(s["pass"] for s in stats)
+    e["oracle"] = {"sample": (f"heads {heads}, " + ("all query rows" if r is None
+                                                     else f"last {r} query rows")),
+                   "seconds": secs, "errors": worst}
+    del q1, k1, q2, k2, g, ws, outs, grads
+    torch.cuda.empty_cache()
+    return e
 
 
 def gpu_arm(args, w):
@@ -352,39 +533,61 @@ def gpu_arm(args, w):
     fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
 
-    f_fwd, f_bwd_metric, f_bwd_work, f_fwd_exact, f_bwd_exact = flop_counts(w)
-    f_bwd_work_exact = f_bwd_exact
+    f_fwd, f_bwd_metric = flop_counts(w)
+    m_fwd, m_bwd = method_flops(w)
     algo = binding.bwd_algorithm(B, H, NQ, NK, d, w.causal, w.grad1)
+    separate = algo == binding.BWD_SEPARATE
+    x_bwd = executed_bwd_flops(w, separate)
     pairs = w.live_pairs_per_head() * B * H
-    if algo == binding.BWD_SEPARATE:
-        # the dK and dQ kernels each recompute S1 and S2 (4d FLOPs per pair) and
-        # add one d x 2 GEMM per gradient set
-        f_bwd_exact = (8 + (8 if w.grad1 else 4)) * pairs * d
+    if separate:
         bwd_name = "streamkl_bwd_sep_kernel (dK + dQ)"
-        bwd_note = "separate dK and dQ kernels, timed together (one API call)"
+        bwd_note = ("separate dK and dQ kernels, timed together (one API call); each "
+                    "regenerates S1 and S2, so they execute 16d FLOPs per pair with both "
+                    "gradient sets against the method's 12d")
     else:
         bwd_name = "streamkl_bwd_kernel"
         bwd_note = "fused kernel; includes the workspace clear and the fp32->bf16 dQ conversion"
     step_flops = f_fwd + f_bwd_metric
     value = world * step_flops / (ms_step * 1e-3) / 1e12
     pk = peaks()
-    sustained = pk["bf16_tflops_sustained"]
-    fwd_tf = f_fwd_exact / (fwd_ms * 1e-3) / 1e12
-    bwd_tf = f_bwd_exact / (bwd_ms * 1e-3) / 1e12
+    sustained, burst = pk["bf16_tflops_sustained"], pk["bf16_tflops"]
+    fwd_tf = m_fwd / (fwd_ms * 1e-3) / 1e12
+    bwd_tf = m_bwd / (bwd_ms * 1e-3) / 1e12
+    bwd_xtf = x_bwd / (bwd_ms * 1e-3) / 1e12
+    unit_note = ("method work on the exact visible (query, key) pairs: forward 4d FLOPs per "
+                 "pair; backward 4d (regenerate S1, S2) + 4d per gradient set")
     kernels = {
-        "streamkl_fwd_kernel": {"ms": fwd_ms, "algorithmic_tflop": f_fwd_exact / 1e12,
-                                "achieved_tflops": fwd_tf, "frac_of_measured_sustained": fwd_tf / sustained},
-        bwd_name: {"ms": bwd_ms, "algorithmic_tflop": f_bwd_exact / 1e12,
+        "streamkl_fwd_kernel": {"ms": fwd_ms, "algorithmic_tflop": m_fwd / 1e12,
+                                "achieved_tflops": fwd_tf,
+                                "frac_of_measured_sustained": fwd_tf / sustained,
+                                "frac_of_measured_burst": fwd_tf / burst},
+        bwd_name: {"ms": bwd_ms, "algorithmic_tflop": m_bwd / 1e12,
                    "achieved_tflops": bwd_tf, "frac_of_measured_sustained": bwd_tf / sustained,
+                   "frac_of_measured_burst": bwd_tf / burst,
+                   "executed_tflop": x_bwd / 1e12, "executed_tflops": bwd_xtf,
+                   "executed_frac_of_measured_sustained": bwd_xtf / sustained,
                    "note": bwd_note},
     }
     dom = bwd_name if bwd_ms >= fwd_ms else "streamkl_fwd_kernel"
     dom_tf = kernels[dom]["achieved_tflops"]
+    traffic = recorded_traffic(w.name, dom)
     roofline = {"bound": "tensor", "kernel": dom, "achieved": dom_tf, "peak": sustained,
-                "unit": "TFLOP/s", "frac": dom_tf / sustained,
-                "traffic": recorded_traffic(w.name, dom),
-                "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a long step)"}
-    if algo == binding.BWD_SEPARATE:
+                "unit": "TFLOP/s", "frac": dom_tf / sustained, "traffic": traffic,
+                "algorithmic": unit_note,
+                "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a long step)",
+                "frac_of_measured_burst": dom_tf / burst}
+    if dom == bwd_name:
+        roofline["executed_tflops"] = bwd_xtf
+        roofline["executed_frac"] = bwd_xtf / sustained
+        if traffic is not None:
+            mb = bwd_min_bytes(w)
+            roofline["traffic_min_bytes"] = mb
+            roofline["traffic_over_min"] = traffic / mb
+            roofline["traffic_ok"] = traffic <= 1.5 * mb
+            if traffic > 1.5 * mb:
+                print(f"warning: {dom} moves {traffic / mb:.2f}x its minimum DRAM bytes "
+                      "(limit 1.5x)", file=sys.stderr)
+    if separate:
         launches_per_step = 1 + (1 if splits > 1 else 0) + 2
     else:
         launches_per_step = 1 + (1 if splits > 1 else 0) + 1 + (2 if w.grad1 else 1)
@@ -394,10 +597,28 @@ def gpu_arm(args, w):
         e2e = e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world)
 
     cpu = None
+    configs = None
     if rank == 0 and not args.no_cpu_baseline and world == 1:
-        v, dt, flops, desc = oracle_sample(w, args.cpu_budget_s)
+        head = host_head((q1, k1, q2, k2, g), 0, 0)
+        v, dt, rows, oo, desc = oracle_sample(w, args.cpu_budget_s, head)
+        gpu = host_head((kl, l1, l2) + grads, 0, 0)
+        main_err = error_stats(w, rows, oo, (gpu[0], gpu[1], gpu[2], gpu[3:]))
         cpu = {"value": v, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": f"{desc}; {dt:.1f} s"}
+               "sample": f"head 0 of the timed run's inputs, {desc}; {dt:.1f} s"}
+        configs = [{"workload": describe(w), "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+                    "fwd_tflops": fwd_tf, "bwd_tflops_method": bwd_tf,
+                    "bwd_tflops_executed": bwd_xtf,
+                    "frac_of_measured_sustained": {"fwd": fwd_tf / sustained,
+                                                   "bwd_method": bwd_tf / sustained},
+                    "oracle": {"sample": f"head 0, last {len(rows)} query rows", "seconds": dt,
+                               "errors": main_err}}]
+        if not args.no_configs:
+            del q1, k1, q2, k2, g, ws, grads
+            torch.cuda.empty_cache()
+            for i, name in enumerate(("tiny", "mid", "splitk", "stress")):
+                if name != w.name:
+                    configs.append(config_entry(synthetic.WORKLOADS[name], binding, synthetic,
+                                                dev, pk, 2000 + i))
 
     extra_hbm = {
         "workspace_bytes": ws_bytes,
@@ -412,27 +633,25 @@ def gpu_arm(args, w):
             "data": "synthetic",
             "config": {"workload": describe(w), "B": B, "H": H, "N_Q": NQ, "N_K": NK, "d": d,
                        "causal": w.causal, "grad1": w.grad1, "splits": splits,
-                       "bwd_algorithm": "separate" if algo == binding.BWD_SEPARATE else "fused",
+                       "bwd_algorithm": "separate" if separate else "fused",
                        "flop_convention": "4 NQ NK d fwd + 8 NQ NK d bwd per head, halved for causal",
                        "l2": "inputs (2 GiB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
             "bwd_tflops_metric": f_bwd_metric / (bwd_ms * 1e-3) / 1e12,
-            # the same times over exact counts: visible (query, key) pairs,
-            # 4d FLOPs per pair forward, 8d (one gradient set) or 12d (both)
-            # backward, i.e. the work the method needs, not what one kernel
-            # design executes
+            # the same times over the method's work on the exact visible pairs
             "visible_pairs": pairs,
-            "fwd_tflops_exact": f_fwd_exact / (fwd_ms * 1e-3) / 1e12,
-            "bwd_tflops_work": f_bwd_work_exact / (bwd_ms * 1e-3) / 1e12,
-            "pct_of_measured_peak": {"value": value / world / pk["bf16_tflops"],
-                                     "fwd": f_fwd / (fwd_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
-                                     "bwd_metric": f_bwd_metric / (bwd_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+            "fwd_tflops_method": fwd_tf,
+            "bwd_tflops_method": bwd_tf,
+            "pct_of_measured_peak": {"value": value / world / burst,
+                                     "fwd": f_fwd / (fwd_ms * 1e-3) / 1e12 / burst,
+                                     "bwd_metric": f_bwd_metric / (bwd_ms * 1e-3) / 1e12 / burst,
                                      "peak": f"{pk['source']} bf16_tflops (burst)"},
             "roofline": roofline, "kernels": kernels,
             "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": launches_per_step * args.steps,
             "extra_hbm": extra_hbm,
+            "configs": configs,
         })
     if world > 1:
         import torch.distributed as dist
@@ -442,15 +661,16 @@ def gpu_arm(args, w):
 
 def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
     """Same metric through the public API with host buffers: every step copies
-    its inputs from pinned host memory and reads the per-row KL back.
+    its inputs from pinned host memory and every result back to pinned host
+    memory (KL, LSE1, LSE2 and the gradients).
 
     A step's batch goes through the API in G groups of (batch, head) slices
     (heads are independent, so this is the same computation), streamed
-    through two device buffers: group i+1's host-to-device copy runs on a
-    second stream while group i computes, so only the first group's copy of
-    the first step is exposed. Every copy is enqueued after the start event
-    and finishes before the group that uses it, so all of them fall inside
-    the timed region."""
+    through two device slots: group u's inputs are copied in on one stream
+    and its results out on another, so group u+1's inputs and group u-1's
+    results move while group u computes. Every copy is enqueued after the
+    start event and the stop event waits for the last one, so all of them
+    fall inside the timed region."""
     import torch
     q1, k1, q2, k2, g = synthetic.make_inputs(w, replica_seed(rank) + 7, dev)
     host_in = [t.cpu().pin_memory() for t in (q1, k1, q2, k2, g)]
@@ -463,25 +683,48 @@ def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
         return t.reshape((bh,) + tuple(t.shape[2:]))[i * per:(i + 1) * per].unsqueeze(0)
 
     host_groups = [[part(t, i) for t in host_in] for i in range(groups)]
-    bufs = [[torch.empty_like(t, device=dev) for t in host_groups[0]] for _ in range(2)]
-    kl_host = torch.empty((w.B, w.H, w.NQ), dtype=torch.float32).pin_memory()
-    kl_groups = [part(kl_host, i) for i in range(groups)]
+    # results on the host: kl, lse1, lse2, then dq2, dk2 (and dq1, dk1)
+    row = torch.empty((w.B, w.H, w.NQ), dtype=torch.float32)
+    host_out = [torch.empty_like(row).pin_memory() for _ in range(3)]
+    host_out += [torch.empty_like(host_in[2]).pin_memory(), torch.empty_like(host_in[3]).pin_memory()]
+    if w.grad1:
+        host_out += [torch.empty_like(host_in[0]).pin_memory(),
+                     torch.empty_like(host_in[1]).pin_memory()]
+    host_out_groups = [[part(t, i) for t in host_out] for i in range(groups)]
+    in_bufs = [[torch.empty_like(t, device=dev) for t in host_groups[0]] for _ in range(2)]
+    out_bufs = [[torch.empty_like(t, device=dev) for t in host_out_groups[0]] for _ in range(2)]
+    sub = host_groups[0]
+    ws_bytes = binding.streamkl_workspace_size(1, per, w.NQ, w.NK, w.d, w.causal, w.grad1)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=dev)
+    status = binding.new_status(dev)
     stream = torch.cuda.current_stream(dev)
-    copy_stream = torch.cuda.Stream(dev)
-    ready = [torch.cuda.Event() for _ in range(2)]
-    free = [torch.cuda.Event() for _ in range(2)]
+    h2d_stream = torch.cuda.Stream(dev)
+    d2h_stream = torch.cuda.Stream(dev)
+    ready = [torch.cuda.Event() for _ in range(2)]     # inputs of a slot copied in
+    in_free = [torch.cuda.Event() for _ in range(2)]   # a slot's inputs consumed
+    done = [torch.cuda.Event() for _ in range(2)]      # a slot's results computed
+    out_free = [torch.cuda.Event() for _ in range(2)]  # a slot's results copied out
+    assert sub[0].shape[1] == per
 
     def h2d(slot, gi):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(free[slot])
-            for hsrc, d in zip(host_groups[gi], bufs[slot]):
+        with torch.cuda.stream(h2d_stream):
+            h2d_stream.wait_event(in_free[slot])
+            for hsrc, d in zip(host_groups[gi], in_bufs[slot]):
                 d.copy_(hsrc, non_blocking=True)
-            ready[slot].record(copy_stream)
+            ready[slot].record(h2d_stream)
+
+    def d2h(slot, gi):
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(done[slot])
+            for d, hdst in zip(out_bufs[slot], host_out_groups[gi]):
+                hdst.copy_(d, non_blocking=True)
+            out_free[slot].record(d2h_stream)
 
     def run(steps):
-        for e in free:
+        for e in in_free + out_free:
             e.record(stream)
-        copy_stream.wait_stream(stream)
+        h2d_stream.wait_stream(stream)
+        d2h_stream.wait_stream(stream)
         units = steps * groups
         h2d(0, 0)
         for u in range(units):
@@ -489,14 +732,21 @@ def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
             if u + 1 < units:
                 h2d(slot ^ 1, (u + 1) % groups)
             stream.wait_event(ready[slot])
-            x = bufs[slot]
-            kl, l1, l2 = binding.streamkl_fwd(*x[:4], w.scale, w.causal)
-            binding.streamkl_bwd(*x[:4], kl, l1, l2, x[4], w.scale, w.causal, grad1=w.grad1)
-            free[slot].record(stream)
-            kl_groups[gi].copy_(kl, non_blocking=True)
+            stream.wait_event(out_free[slot])
+            x, o = in_bufs[slot], out_bufs[slot]
+            binding.streamkl_fwd(*x[:4], w.scale, w.causal, out=tuple(o[:3]), workspace=ws,
+                                 dev_status=status)
+            binding.streamkl_bwd(*x[:4], *o[:3], x[4], w.scale, w.causal, grad1=w.grad1,
+                                 out=tuple(o[3:]) + ((None, None) if not w.grad1 else ()),
+                                 workspace=ws, dev_status=status)
+            in_free[slot].record(stream)
+            done[slot].record(stream)
+            d2h(slot, gi)
+        stream.wait_stream(d2h_stream)
 
     run(max(1, args.warmup))
     torch.cuda.synchronize(dev)
+    binding.raise_on_device_status(status, "e2e warm-up")
     barrier()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
@@ -504,14 +754,16 @@ def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
     b.record(stream)
     torch.cuda.synchronize(dev)
     barrier()
+    binding.raise_on_device_status(status, "e2e")
     ms = max_over_ranks(a.elapsed_time(b) / args.steps, dev)
     h2d_bytes = sum(t.numel() * t.element_size() for t in host_in)
-    d2h = kl_host.numel() * 4
+    d2h_bytes = sum(t.numel() * t.element_size() for t in host_out)
     return {"value": world * step_flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h,
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
+            "results_copied": "kl, lse1, lse2, dq2, dk2" + (", dq1, dk1" if w.grad1 else ""),
             "overlap": f"each step's batch in {groups} groups of {per} (batch, head) slices through "
-                       "two device buffers: a group's host-to-device copy runs on a second stream "
-                       "while the previous group computes; the first group's copy is exposed",
+                       "two device slots: a group's inputs are copied in on one stream and its "
+                       "results out on another while the neighbouring group computes",
             "api": "attention_kl_loss_gb300.streamkl_fwd/streamkl_bwd (ctypes over the C ABI)"}
 
 

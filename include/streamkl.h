@@ -178,8 +178,12 @@ streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, con
  * streamkl_fwd. Calls without splits do not touch the scratch.
  *
  * The first call that uses the scratch on a device looks up its device
- * address (with that device current) and caches it; make that first call
- * before any stream capture. All calls on a device share the one array and
+ * address (with that device current) and caches it together with the current
+ * driver context; make that first call before any stream capture. A call
+ * made in another context than the cached one (after cudaDeviceReset, which
+ * drops the library's module and the array with it, or with a non-primary
+ * context current) looks the address up again, so the first such call should
+ * also come before any capture. All calls on a device share the one array and
  * each leaves its partial states in it; nothing there needs clearing because
  * every call writes all the states it reads, but calls whose kernels may
  * overlap on the GPU (different streams, other host threads) race on it and

@@ -214,6 +214,8 @@ def head_backward(q1, k1, q2, k2, scale: float, causal: bool, g, grad1: bool,
     q1, k1, q2, k2 = (_f64(x) for x in (q1, k1, q2, k2))
     g = _f64(g)
     n_q, n_k = q1.shape[0], k1.shape[0]
+    if causal and n_q > n_k:
+        raise ValueError("causal needs N_Q <= N_K (bottom-right alignment)")
     rows = np.arange(n_q) if rows is None else np.asarray(rows, dtype=np.int64)
     dq2 = np.zeros((len(rows), q2.shape[1]))
     dk2 = np.zeros_like(k2)

@@ -1,11 +1,11 @@
 """Sweeps behind the design choices (run on one GPU, prints markdown tables).
 
-    python -m attention_kl_loss_gb300.sweep algo      # fused vs separate backward
-    python -m attention_kl_loss_gb300.sweep decode    # split-K on/off for few query rows
-    python -m attention_kl_loss_gb300.sweep context   # context length 4K .. 512K
-    python -m attention_kl_loss_gb300.sweep dqsplit   # backward dQ key split on/off
-    python -m attention_kl_loss_gb300.sweep configs   # the named workloads, fwd and bwd
-    python -m attention_kl_loss_gb300.sweep dkpersist # persistent dK kernel off/on, short queries
+    python sweep.py algo      # fused vs separate backward
+    python sweep.py decode    # split-K on/off for few query rows
+    python sweep.py context   # context length 4K .. 512K
+    python sweep.py dqsplit   # backward dQ key split on/off
+    python sweep.py configs   # the named workloads, fwd and bwd
+    python sweep.py dkpersist # persistent dK kernel off/on, short queries
 
 Every point is timed through the C ABI with CUDA events on the current stream,
 inputs resident in device memory, one untimed call first, the median of
@@ -17,11 +17,17 @@ forward; backward 8d per pair and gradient set (two score recomputes, dK, dQ).
 from __future__ import annotations
 
 import argparse
+import os
 import statistics
+import sys
 
 import torch
 
-from . import binding, synthetic
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from attention_kl_loss_gb300 import binding, synthetic  # noqa: E402
 
 
 def _time(fn, reps: int) -> float:

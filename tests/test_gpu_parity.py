@@ -382,14 +382,38 @@ def test_split_invariance(splits):
     assert torch.allclose(kl, ref_kl, rtol=1e-4, atol=1e-5)
 
 
-def sampled_check(w, heads, rows, key_sets, seed=0, algo=None):
+_LONG_SWEEP_CACHE = {}
+
+
+def _oracle_all_rows_backward(w, seed, b, hh, h, g):
+    """The oracle's gradients of one head summed over every query row (cached:
+    the same seeded inputs serve both backward algorithms)."""
+    key = (w.name, seed, b, hh)
+    if key not in _LONG_SWEEP_CACHE:
+        _LONG_SWEEP_CACHE[key] = orc.head_backward(*h, w.scale, w.causal, g, w.grad1)
+    return _LONG_SWEEP_CACHE[key]
+
+
+def sampled_check(w, heads, rows, key_sets, seed=0, algo=None, long_sweep=None):
     """Full-size GPU run; oracle on sampled heads/rows/keys.
 
     rows: query rows whose KL, lse and dQ are compared.
     key_sets: key index arrays whose dK is compared; the oracle sums over every
     query row that can see them.
+    long_sweep: optional ((b, h), keys): dK of these keys of that head against
+    the oracle summed over all N_Q query rows (under the causal mask the first
+    keys are seen by every row, so their dK is the kernel's longest
+    accumulation).
     """
     ins, (kl, l1, l2), grads = run(w, seed, algo=algo)
+    if long_sweep is not None:
+        (b, hh), keys = long_sweep
+        h = [host(t[b, hh]) for t in ins[:4]]
+        g = ins[4][b, hh].cpu().numpy().astype(np.float64)
+        og = _oracle_all_rows_backward(w, seed, b, hh, h, g)
+        assert_grad(host(grads[1][b, hh])[keys], og[1][keys], "dk2 (all query rows)")
+        if w.grad1:
+            assert_grad(host(grads[3][b, hh])[keys], og[3][keys], "dk1 (all query rows)")
     g_all = ins[4]
     n_sets = 4 if w.grad1 else 2
     for (b, hh) in heads:
@@ -450,6 +474,10 @@ def test_splitk_workload_full_size(algo):
 
 @pytest.mark.parametrize("algo", ALGOS)
 def test_causal64k_workload_full_size(algo):
+    """Sampled rows and the last keys on two heads; keys 0..127 of head 0,
+    which every one of the 65,536 query rows sees, against the oracle summed
+    over all rows (the dK kernel's full 1,024-step sweep)."""
     w = synthetic.WORKLOADS["causal64k"]
     sampled_check(w, heads=[(0, 0), (0, 31)], rows=_rows(w.NQ, 256, 3),
-                  key_sets=[np.arange(w.NK - 256, w.NK)], algo=algo)
+                  key_sets=[np.arange(w.NK - 256, w.NK)], algo=algo,
+                  long_sweep=((0, 0), np.arange(0, 128)))

@@ -300,3 +300,116 @@ def test_planted_mistakes_are_caught(monkeypatch, mutation):
         monkeypatch.setattr(orc, "dkl_ds1", lambda p1, lr, kl: lr - kl[:, None])
     with pytest.raises(AssertionError):
         _fd_check(5, 7, 4, True, seed=3)
+
+
+def _batched_case():
+    """B = 2, H = 3, N_Q != N_K, four distinct tensors, g varying per (b, h, row)."""
+    rng = np.random.default_rng(41)
+    B, H, n_q, n_k, d = 2, 3, 6, 9, 5
+    q1 = rng.standard_normal((B, H, n_q, d)) * 1.3
+    k1 = rng.standard_normal((B, H, n_k, d)) * 1.1
+    q2 = rng.standard_normal((B, H, n_q, d)) * 0.9
+    k2 = rng.standard_normal((B, H, n_k, d)) * 1.2
+    g = rng.standard_normal((B, H, n_q))
+    return q1, k1, q2, k2, g, 0.55
+
+
+def _torch_slice(q1, k1, q2, k2, g, scale, causal):
+    """KL, lse1, lse2 rows and the four gradients of sum_i g_i KL_i for one
+    (b, h) slice, by torch fp64 autograd over sliced (not masked) rows."""
+    t = [torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q1, k1, q2, k2)]
+    n_q, n_k = q1.shape[0], k1.shape[0]
+    kls = []
+    for i in range(n_q):
+        n = n_k if not causal else i + 1 + (n_k - n_q)
+        lp1 = torch.log_softmax(scale * t[1][:n] @ t[0][i], dim=-1)
+        lp2 = torch.log_softmax(scale * t[3][:n] @ t[2][i], dim=-1)
+        kls.append(torch.nn.functional.kl_div(lp2, lp1, reduction="sum", log_target=True))
+    kl = torch.stack(kls)
+    (kl * torch.tensor(g)).sum().backward()
+    # order of the oracle's outputs: dq2, dk2, dq1, dk1
+    return kl.detach().numpy(), [t[2].grad.numpy(), t[3].grad.numpy(), t[0].grad.numpy(),
+                                 t[1].grad.numpy()]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_batched_forward_and_backward_per_slice(causal):
+    """The batched [B, H] entry points against routes that share nothing with
+    the oracle: scipy row loops for KL and LSE, torch fp64 autograd for the
+    four gradients, slice by slice."""
+    q1, k1, q2, k2, g, scale = _batched_case()
+    B, H, n_q, _ = q1.shape
+    n_k = k1.shape[2]
+    kl, lse1, lse2 = orc.forward(q1, k1, q2, k2, scale, causal)
+    grads = orc.backward(q1, k1, q2, k2, scale, causal, g, True)
+    assert kl.shape == lse1.shape == lse2.shape == (B, H, n_q)
+    assert grads[0].shape == grads[2].shape == q1.shape
+    assert grads[1].shape == grads[3].shape == k1.shape
+    for b in range(B):
+        for h in range(H):
+            for i in range(n_q):
+                n = n_k if not causal else i + 1 + (n_k - n_q)
+                s1 = scale * (k1[b, h, :n] @ q1[b, h, i])
+                s2 = scale * (k2[b, h, :n] @ q2[b, h, i])
+                assert kl[b, h, i] == pytest.approx(
+                    sst.entropy(sps.softmax(s1), sps.softmax(s2)), rel=1e-10, abs=1e-13)
+                assert lse1[b, h, i] == pytest.approx(sps.logsumexp(s1), rel=1e-13)
+                assert lse2[b, h, i] == pytest.approx(sps.logsumexp(s2), rel=1e-13)
+            _, ref = _torch_slice(q1[b, h], k1[b, h], q2[b, h], k2[b, h], g[b, h], scale, causal)
+            for got, want in zip(grads, ref):
+                np.testing.assert_allclose(got[b, h], want, rtol=1e-9, atol=1e-13)
+
+
+def test_batched_one_gradient_set_and_head_subset():
+    """grad1 = False returns only configuration 1's gradients; a head subset
+    leaves the other heads NaN and is exact on its own heads."""
+    q1, k1, q2, k2, g, scale = _batched_case()
+    full = orc.backward(q1, k1, q2, k2, scale, True, g, True)
+    one = orc.backward(q1, k1, q2, k2, scale, True, g, False)
+    assert one[2] is None and one[3] is None
+    np.testing.assert_array_equal(one[0], full[0])
+    np.testing.assert_array_equal(one[1], full[1])
+    sub = orc.backward(q1, k1, q2, k2, scale, True, g, True, heads=[(1, 2)])
+    fsub = orc.forward(q1, k1, q2, k2, scale, True, heads=[(1, 2)])
+    for x, y in zip(sub, full):
+        np.testing.assert_array_equal(x[1, 2], y[1, 2])
+        assert np.all(np.isnan(x[0])) and np.all(np.isnan(x[1, :2]))
+    assert np.all(np.isnan(fsub[0][0])) and np.all(np.isfinite(fsub[0][1, 2]))
+
+
+@pytest.mark.parametrize("mutation", ["q1_q2_k1_k2", "swap_student_teacher", "swap_lse_outputs",
+                                      "g_other_head", "dq_dk_sets_swapped"])
+def test_batched_planted_mistakes_are_caught(monkeypatch, mutation):
+    """Plausible slips at the batched entry points' call sites (arguments or
+    outputs in the wrong order, the wrong slice of g) fail the per-slice pin."""
+    real_f, real_b = orc.head_forward, orc.head_backward
+    if mutation == "q1_q2_k1_k2":  # N_Q != N_K: the shapes no longer line up
+        monkeypatch.setattr(orc, "head_forward",
+                            lambda q1, k1, q2, k2, *a, **k: real_f(q1, q2, k1, k2, *a, **k))
+    elif mutation == "swap_student_teacher":
+        monkeypatch.setattr(orc, "head_forward",
+                            lambda q1, k1, q2, k2, *a, **k: real_f(q2, k2, q1, k1, *a, **k))
+    elif mutation == "swap_lse_outputs":
+        def f(*a, **k):
+            kl, l1, l2 = real_f(*a, **k)
+            return kl, l2, l1
+        monkeypatch.setattr(orc, "head_forward", f)
+    elif mutation == "g_other_head":
+        def b(q1, k1, q2, k2, scale, causal, g, grad1, rows=None):
+            return real_b(q1, k1, q2, k2, scale, causal, g[::-1].copy(), grad1, rows)
+        monkeypatch.setattr(orc, "head_backward", b)
+    else:
+        def b(*a, **k):
+            dq2, dk2, dq1, dk1 = real_b(*a, **k)
+            return dq1, dk1, dq2, dk2
+        monkeypatch.setattr(orc, "head_backward", b)
+    with pytest.raises((AssertionError, ValueError)):
+        test_batched_forward_and_backward_per_slice(True)
+
+
+def test_backward_rejects_causal_with_more_queries_than_keys():
+    q1, k1, q2, k2 = _case(43, 9, 5, 4)
+    with pytest.raises(ValueError):
+        orc.head_backward(q1, k1, q2, k2, 0.5, True, np.ones(9), True)
+    with pytest.raises(ValueError):
+        orc.head_forward(q1, k1, q2, k2, 0.5, True)

@@ -18,6 +18,7 @@ import pytest
 import torch
 
 from attention_kl_loss_gb300 import binding, synthetic
+from oracle import streamkl_oracle as orc
 
 KL_ABS, KL_REL, LSE_REL = 2e-3, 1e-2, 1e-4
 SCRATCH_BYTES = 16 << 20
@@ -78,3 +79,36 @@ def test_noalloc_forward_matches_workspace_forward_on_two_calls(lib):
         assert _rel_l2(lse1, ref[1]) <= LSE_REL
         assert _rel_l2(lse2, ref[2]) <= LSE_REL
     assert np.isfinite(float(kl.sum()))
+
+
+@pytest.mark.gpu
+def test_noalloc_automatic_split_against_the_oracle(lib):
+    """num_splits = 0 (the library's own split choice, the normal way to call
+    it) on a decode-like shape where that choice splits the keys, so the
+    built-in scratch is used; outputs against the fp64 oracle and against the
+    workspace forward."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    dev = torch.device("cuda")
+    w = synthetic.custom("noalloc_decode", B=1, H=4, NQ=64, NK=65536, d=128, causal=True,
+                         noise=0.3)
+    splits = binding.choose_splits(w.B, w.H, w.NQ, w.NK, w.d, w.causal)
+    assert splits > 1
+    assert 0 < binding.streamkl_fwd_workspace_size(w.B, w.H, w.NQ, w.NK, w.d, w.causal,
+                                                   0) <= SCRATCH_BYTES
+    q1, k1, q2, k2, _ = synthetic.make_inputs(w, 13, dev)
+    out = tuple(torch.full((w.B, w.H, w.NQ), float("nan"), device=dev) for _ in range(3))
+    status = binding.new_status(dev)
+    binding.streamkl_fwd_noalloc(q1, k1, q2, k2, out, w.scale, w.causal, num_splits=0,
+                                 dev_status=status)
+    binding.raise_on_device_status(status, "streamkl_fwd_noalloc")
+    ref = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, num_splits=0)
+    kl, lse1, lse2 = out
+    assert _close(kl, ref[0])
+    h = [t.float().cpu().numpy().astype(np.float64) for t in (q1, k1, q2, k2)]
+    okl, ol1, ol2 = orc.forward(*h, w.scale, w.causal)
+    err = np.abs(kl.cpu().numpy().astype(np.float64) - okl)
+    assert np.all(err <= KL_ABS + KL_REL * np.abs(okl))
+    for got, want in ((lse1, ol1), (lse2, ol2)):
+        g = got.cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(g - want) / np.linalg.norm(want) <= LSE_REL
