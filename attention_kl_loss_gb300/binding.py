@@ -7,6 +7,7 @@ must have been built in-tree (``__graft_entry__.build()`` or
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -21,8 +22,14 @@ STREAMKL_ERR_INVALID_ARG = 1
 STREAMKL_ERR_UNSUPPORTED = 2
 STREAMKL_ERR_CUDA = 3
 STREAMKL_ERR_TIMEOUT = 4
+STREAMKL_ERR_DEVICE_CHECK = 5
 
-_lib: Optional[ctypes.CDLL] = None
+_STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT",
+                 5: "DEVICE_CHECK"}
+
+# loaded libraries: False = release build, True = debug build (device checks)
+_libs: dict = {}
+_use_debug = False
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -45,6 +52,7 @@ _SIGNATURES = {
     "streamkl_bwd_reverse": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P, _P, _P,
                                   _P, _P, _P, _P, _Z, _P, _P]),
     "streamkl_selftest_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
+    "streamkl_selftest_device_check": (_I, [_P, _P]),
     "streamkl_bwd_algorithm": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "streamkl_set_bwd_algorithm": (_I, [_I]),
     "streamkl_bwd_dq_splits": (_I, [_I, _I, _I, _I, _I, _I, _I]),
@@ -63,31 +71,50 @@ _SIGNATURES = {
 class StreamKLError(RuntimeError):
     def __init__(self, status: int, where: str, detail: str = ""):
         self.status = status
-        name = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "CUDA", 4: "TIMEOUT"}.get(status, "?")
+        name = _STATUS_NAMES.get(status, "?")
         super().__init__(f"{where}: STREAMKL_ERR_{name} ({status}) {detail}".strip())
 
 
-def library_path() -> str:
-    return _build.lib_path()
+def library_path(debug: bool = False) -> str:
+    return _build.lib_path(debug)
 
 
-def load() -> ctypes.CDLL:
-    """Load the in-tree library (raises if it has not been built)."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    path = library_path()
+def _load_variant(debug: bool) -> ctypes.CDLL:
+    if debug in _libs:
+        return _libs[debug]
+    path = library_path(debug)
     if not os.path.exists(path):
-        raise RuntimeError(
-            f"StreamKL CUDA library not found at {path}; build it with "
-            "`python -c 'import __graft_entry__ as g; g.build()'`")
+        how = ("`python -m attention_kl_loss_gb300.build --debug`" if debug
+               else "`python -c 'import __graft_entry__ as g; g.build()'`")
+        raise RuntimeError(f"StreamKL CUDA library not found at {path}; build it with {how}")
     lib = ctypes.CDLL(path)
     for name, (res, args) in _SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
+    _libs[debug] = lib
     return lib
+
+
+def load(debug: Optional[bool] = None) -> ctypes.CDLL:
+    """Load the in-tree library (raises if it has not been built): the one the
+    binding's calls use (the debug build inside ``use_debug_library()``), or
+    the release / debug build when ``debug`` is given."""
+    return _load_variant(_use_debug if debug is None else debug)
+
+
+@contextlib.contextmanager
+def use_debug_library():
+    """Route this module's calls to the debug build (device-side range checks
+    that report STREAMKL_ERR_DEVICE_CHECK) for the duration of the block."""
+    global _use_debug
+    prev = _use_debug
+    lib = _load_variant(True)
+    _use_debug = True
+    try:
+        yield lib
+    finally:
+        _use_debug = prev
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -374,9 +401,23 @@ def selftest_wait_timeout(timeout_us: int = 20000, dev_status=None, stream=None)
     return status
 
 
+def selftest_device_check(dev_status=None, stream=None) -> torch.Tensor:
+    """Run the range-check self-test kernel; returns the status tensor
+    (STREAMKL_ERR_DEVICE_CHECK from the debug build, unchanged from the
+    release build)."""
+    lib = load()
+    status = dev_status if dev_status is not None else new_status()
+    _check(lib.streamkl_selftest_device_check(_ptr(status), _stream_handle(stream)),
+           "streamkl_selftest_device_check")
+    return status
+
+
 def raise_on_device_status(dev_status: torch.Tensor, where: str = "kernel"):
     """Synchronise and raise if a kernel recorded a failure in ``dev_status``."""
     torch.cuda.synchronize(dev_status.device)
     v = int(dev_status.item())
     if v != 0:
-        raise StreamKLError(v, where, "a bounded wait inside the kernel gave up")
+        why = {STREAMKL_ERR_TIMEOUT: "a bounded wait inside the kernel gave up",
+               STREAMKL_ERR_INVALID_ARG: "malformed sequence offsets or causal rows without a key",
+               STREAMKL_ERR_DEVICE_CHECK: "a device-side range check failed (debug build)"}
+        raise StreamKLError(v, where, why.get(v, "kernel failure"))

@@ -2,6 +2,12 @@
 
 Every translation unit is compiled for sm_103a only (GB300), in parallel, then
 linked with the static CUDA runtime. Nothing is installed outside the tree.
+
+``build(debug=True)`` builds ``_lib/libstreamkl_debug.so`` from the same
+sources with STREAMKL_DEVICE_CHECKS defined: the kernels then check the
+operands of every TMA copy, TMEM access and mbarrier against their layout
+and report a failed check as STREAMKL_ERR_DEVICE_CHECK in the caller's
+status word instead of issuing the access.
 """
 from __future__ import annotations
 
@@ -16,7 +22,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "libstreamkl.so"
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_sep.cu"]
+DEBUG_LIB_NAME = "libstreamkl_debug.so"
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_sep.cu", "bwd_short.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]
@@ -30,8 +37,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found (set NVCC or put CUDA's bin on PATH)")
 
 
-def lib_path() -> str:
-    return os.path.join(OUT_DIR, LIB_NAME)
+def lib_path(debug: bool = False) -> str:
+    return os.path.join(OUT_DIR, DEBUG_LIB_NAME if debug else LIB_NAME)
 
 
 def _stale(target: str, deps) -> bool:
@@ -41,19 +48,23 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) -> str:
-    """Compile (if stale) and return the library path."""
+def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False,
+          debug: bool = False) -> str:
+    """Compile (if stale) and return the library path (the debug build with
+    device-side range checks when ``debug``)."""
     os.makedirs(OUT_DIR, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(ROOT, "include", "streamkl.h"))
     objs = []
     jobs = []
+    tag = "_debug" if debug else ""
+    extra = ["-DSTREAMKL_DEVICE_CHECKS"] if debug else []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(OUT_DIR, src.replace(".cu", ".o"))
+        o = os.path.join(OUT_DIR, src.replace(".cu", f"{tag}.o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
-            cmd = [nvcc(), *ARCH, *FLAGS, "-c", s, "-o", o]
+            cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", s, "-o", o]
             if ptxas_info:
                 cmd += ["-Xptxas", "-v"]
             jobs.append(cmd)
@@ -68,7 +79,7 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
                 sys.stderr.write(p.stdout + p.stderr)
             if p.returncode != 0:
                 raise RuntimeError(f"nvcc failed: {' '.join(cmd)}")
-    lib = lib_path()
+    lib = lib_path(debug)
     if force or _stale(lib, objs):
         cmd = [nvcc(), *ARCH, "-shared", "-o", lib, *objs]
         p = subprocess.run(cmd, capture_output=True, text=True)
@@ -79,4 +90,5 @@ def build(verbose: bool = False, ptxas_info: bool = False, force: bool = False) 
 
 
 if __name__ == "__main__":
-    print(build(verbose=True, ptxas_info="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose=True, ptxas_info="-v" in sys.argv, force="-f" in sys.argv,
+                debug="--debug" in sys.argv))

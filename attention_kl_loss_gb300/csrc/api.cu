@@ -160,15 +160,22 @@ int forced_algo() {
   return v;
 }
 
-// Automatic choice, from the fused-vs-separate sweep on GB300: the separate
-// kernels are at least as fast on every shape measured (within 0.5 % on the
-// short-query, long-key shapes where the fused kernel's single pass over the
-// keys comes closest), so the fused kernel runs only when asked for.
+// The fused algorithm runs the short-sweep kernel (persistent grid, dQ kept
+// on chip per batch-head) when the query rows fit one 64-row tile at d = 128,
+// and the kernel with one CTA per key tile and per-tile dQ reductions
+// otherwise.
+bool short_sweep(int NQ, int d) { return d == 128 && NQ <= skl::kShortMaxQ; }
+
+// Automatic choice, from the fused-vs-separate sweep on GB300: the fused
+// short-sweep kernel for decode-like shapes (at most 64 query rows at
+// d = 128, where it reads the keys once against the separate kernels'
+// twice), the separate kernels everywhere else (at least as fast as the
+// per-key-tile fused kernel on every other shape measured).
 int bwd_algo_impl(int B, int H, int NQ, int NK, int d, int grad1) {
   const int forced = forced_algo();
   if (forced >= 0) return forced;
-  (void)B, (void)H, (void)NQ, (void)NK, (void)d, (void)grad1;
-  return 0;
+  (void)B, (void)H, (void)NK, (void)grad1;
+  return short_sweep(NQ, d) ? 1 : 0;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -336,6 +343,7 @@ const char* streamkl_status_string(streamkl_status s) {
     case STREAMKL_ERR_UNSUPPORTED: return "STREAMKL_ERR_UNSUPPORTED";
     case STREAMKL_ERR_CUDA: return "STREAMKL_ERR_CUDA";
     case STREAMKL_ERR_TIMEOUT: return "STREAMKL_ERR_TIMEOUT";
+    case STREAMKL_ERR_DEVICE_CHECK: return "STREAMKL_ERR_DEVICE_CHECK";
   }
   return "STREAMKL_ERR_UNKNOWN";
 }
@@ -601,8 +609,10 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
     return fail(STREAMKL_ERR_INVALID_ARG, "backward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
 
   const int BH = B * H;
-  // the separate kernels move 64-row boxes, the fused one 128-row boxes
-  const int box_rows = algo == 0 ? 64 : skl::kBlockM;
+  const bool short_kernel = algo == 1 && short_sweep(NQ, d);
+  // the separate and short-sweep kernels move 64-row boxes, the per-key-tile
+  // fused one 128-row boxes
+  const int box_rows = (algo == 0 || short_kernel) ? 64 : skl::kBlockM;
   CUtensorMap mq1, mk1, mq2, mk2;
   if ((st = make_map(&mq1, q1, BH, NQ, d, "q1", box_rows)) != STREAMKL_OK) return st;
   if ((st = make_map(&mk1, k1, BH, NK, d, "k1", box_rows)) != STREAMKL_OK) return st;
@@ -645,6 +655,41 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   cudaError_t e = cudaMemsetAsync(workspace, 0, need, s);
   if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
   const size_t one = need / (grad1 ? 2 : 1);
+  const long long n = static_cast<long long>(BH) * NQ * d;
+  if (short_kernel) {
+    skl::BwdShortArgs a{};
+    a.tm_q1 = &mq1;
+    a.tm_k1 = &mk1;
+    a.tm_q2 = &mq2;
+    a.tm_k2 = &mk2;
+    a.BH = BH;
+    a.NQ = NQ;
+    a.NK = NK;
+    a.causal = causal;
+    a.grad1 = grad1;
+    a.grad2 = grad2;
+    a.scale = scale;
+    a.kl = kl;
+    a.lse1 = lse1;
+    a.lse2 = lse2;
+    a.g = dkl;
+    a.dk2 = dk2;
+    a.dk1 = dk1;
+    a.dq2acc = static_cast<float*>(workspace);
+    a.dq1acc = grad1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + one) : nullptr;
+    a.ctas = num_sms();
+    a.dev_status = dev_status;
+    a.timeout_ns = wait_timeout_ns();
+    e = skl::launch_bwd_short(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    e = skl::launch_dq_convert(a.dq2acc, dq2, n, s);
+    if (e != cudaSuccess) return cuda_fail(e, "dq2 convert launch");
+    if (grad1) {
+      e = skl::launch_dq_convert(a.dq1acc, dq1, n, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dq1 convert launch");
+    }
+    return STREAMKL_OK;
+  }
   skl::BwdArgs a{};
   a.tm_q1 = &mq1;
   a.tm_k1 = &mk1;
@@ -669,7 +714,6 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   a.timeout_ns = wait_timeout_ns();
   e = skl::launch_bwd(a, s);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-  const long long n = static_cast<long long>(BH) * NQ * d;
   e = skl::launch_dq_convert(a.dq2acc, dq2, n, s);
   if (e != cudaSuccess) return cuda_fail(e, "dq2 convert launch");
   if (grad1) {
@@ -816,6 +860,14 @@ streamkl_status streamkl_bwd_varlen(const void* q1, const void* k1, const void* 
   a.timeout_ns = wait_timeout_ns();
   cudaError_t e = skl::launch_bwd_separate(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return STREAMKL_OK;
+}
+
+streamkl_status streamkl_selftest_device_check(int* dev_status, void* stream) {
+  g_err[0] = '\0';
+  if (!dev_status) return fail(STREAMKL_ERR_INVALID_ARG, "dev_status must be non-NULL");
+  cudaError_t e = skl::launch_check_selftest(dev_status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
   return STREAMKL_OK;
 }
 

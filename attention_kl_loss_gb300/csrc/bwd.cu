@@ -106,23 +106,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
   volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
 
+  // debug build: the layout's regions (TMEM fields are set once allocated)
+  CheckCtx ck{sb, sb + L::OFF_DS2, sb + L::OFF_BAR, sb + L::OFF_BAR + L::NBAR * 8, 0, 0,
+              abort_flag, dev_status};
   if (threadIdx.x == 0) {
-    mbar_init(k_full, 1);
-    for (int s = 0; s < L::QSTAGES; ++s) {
-      mbar_init(q_full(s), 1);
-      mbar_init(q_empty(s), 1);
-    }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 8);
-    mbar_init(ds_full, 8);
-    mbar_init(ds_free, 1);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, 8);
-    mbar_init(dk_full, 1);
-    mbar_init(drain, 1);
     *abort_flag = 0;
-    // a failure recorded earlier (this launch or a previous one) skips the work
-    *skip_flag = *reinterpret_cast<volatile int*>(dev_status) != 0;
+    bool lay_ok = true;
+    if (kDeviceChecks) {  // every barrier address inside the barrier region
+      lay_ok = check_bar(ck, k_full, __LINE__) && check_bar(ck, s_full, __LINE__) &&
+               check_bar(ck, s_free, __LINE__) && check_bar(ck, ds_full, __LINE__) &&
+               check_bar(ck, ds_free, __LINE__) && check_bar(ck, dq_full, __LINE__) &&
+               check_bar(ck, dq_free, __LINE__) && check_bar(ck, dk_full, __LINE__) &&
+               check_bar(ck, drain, __LINE__);
+      for (int s = 0; s < L::QSTAGES; ++s)
+        lay_ok = lay_ok && check_bar(ck, q_full(s), __LINE__) && check_bar(ck, q_empty(s), __LINE__);
+    }
+    if (lay_ok) {
+      mbar_init(k_full, 1);
+      for (int s = 0; s < L::QSTAGES; ++s) {
+        mbar_init(q_full(s), 1);
+        mbar_init(q_empty(s), 1);
+      }
+      mbar_init(s_full, 1);
+      mbar_init(s_free, 8);
+      mbar_init(ds_full, 8);
+      mbar_init(ds_free, 1);
+      mbar_init(dq_full, 1);
+      mbar_init(dq_free, 8);
+      mbar_init(dk_full, 1);
+      mbar_init(drain, 1);
+    }
+    // a failure recorded earlier (this launch or a previous one), or a
+    // failed layout check, skips the work
+    *skip_flag = !lay_ok || *reinterpret_cast<volatile int*>(dev_status) != 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -141,10 +157,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   if (*skip_flag) n_iter = 0;
   const WaitCtx wc{abort_flag, dev_status, timeout_ns};
+  ck.tmem = tmem;
+  ck.tmem_cols = 512;
+  const int z_hi = static_cast<int>(gridDim.y);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_iter > 0) {
+    bool k_ok = true;
+    if (kDeviceChecks && lane == 0 && n_iter > 0)
+      for (int b = 0; b < L::KB; ++b)
+        k_ok = k_ok &&
+               check_tma(ck, sb + L::OFF_K1 + b * 16384, 16384, k_full, b * 64, D, kb * kBlockN,
+                         NK, kBlockN, bh, z_hi, __LINE__) &&
+               check_tma(ck, sb + L::OFF_K2 + b * 16384, 16384, k_full, b * 64, D, kb * kBlockN,
+                         NK, kBlockN, bh, z_hi, __LINE__);
+    if (lane == 0 && n_iter > 0 && k_ok) {
       mbar_arrive_expect_tx(k_full, 2 * L::TILE);
 #pragma unroll
       for (int b = 0; b < L::KB; ++b) {
@@ -156,9 +183,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int s = it % L::QSTAGES;
         const uint32_t ph = (it / L::QSTAGES) & 1;
         if (!wait_bounded(q_empty(s), ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(q_full(s), 2 * L::TILE);
         const int qrow = (qb0 + it) * kBlockM;
         const uint32_t dst = sb + L::OFF_Q + s * 2 * L::TILE;
+        bool q_ok = true;
+        if (kDeviceChecks)
+          for (int b = 0; b < L::KB; ++b)
+            q_ok = q_ok &&
+                   check_tma(ck, dst + b * 16384, 16384, q_full(s), b * 64, D, qrow, NQ, kBlockM,
+                             bh, z_hi, __LINE__) &&
+                   check_tma(ck, dst + L::TILE + b * 16384, 16384, q_full(s), b * 64, D, qrow, NQ,
+                             kBlockM, bh, z_hi, __LINE__);
+        if (!q_ok) break;
+        mbar_arrive_expect_tx(q_full(s), 2 * L::TILE);
 #pragma unroll
         for (int b = 0; b < L::KB; ++b) {
           tma_load_3d(dst + b * 16384, &tm_q1, q_full(s), b * 64, qrow, bh);
@@ -176,7 +212,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_dk = idesc_bf16(kBlockN, D, 1, 1);
       constexpr uint32_t id_dq = idesc_bf16(kBlockM, D, 0, 1);
       constexpr uint32_t id_dqt = idesc_bf16(D, kBlockM, 1, 0);
-      bool ok = wait_bounded(k_full, 0, wc);
+      // S, dK and dQ accumulators inside the allocation (dQ^T: lanes = d)
+      bool ok = check_tmem(ck, tmem + L::COL_S1, 128, 128, __LINE__) &&
+                check_tmem(ck, tmem + L::COL_S2, 128, 128, __LINE__) &&
+                check_tmem(ck, tmem + L::COL_DK2, 128, D, __LINE__) &&
+                (!GRAD1 || check_tmem(ck, tmem + L::COL_DK1, 128, D, __LINE__)) &&
+                check_tmem(ck, tmem + L::COL_DQ2, L::DQT ? D : 128, L::DQT ? kBlockM : D, __LINE__) &&
+                (!GRAD1 || check_tmem(ck, tmem + L::COL_DQ1, L::DQT ? D : 128,
+                                      L::DQT ? kBlockM : D, __LINE__));
+      ok = ok && wait_bounded(k_full, 0, wc);
       for (int it = 0; ok && it < n_iter; ++it) {
         const int s = it % L::QSTAGES;
         const uint32_t ph = (it / L::QSTAGES) & 1;
@@ -262,6 +306,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       const int lim = causal ? min(NK, qrow + 1 + off) : NK;
       if (!(ok = wait_bounded(s_full, par, wc))) break;
+      if (!(ok = check_tmem(ck, tmem + lane_off + L::COL_S1 + wg * 64, 32, 64, __LINE__) &&
+                 check_tmem(ck, tmem + lane_off + L::COL_S2 + wg * 64, 32, 64, __LINE__)))
+        break;
       tc_fence_after();
       float a[64], b[64];
       tmem_ld32(tmem + lane_off + L::COL_S1 + wg * 64, *reinterpret_cast<float(*)[32]>(&a[0]));
@@ -321,6 +368,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float v[32];
+            if (!check_tmem(ck, tmem + lane_off + col + h * 32, 32, 32, __LINE__)) continue;
             tmem_ld32(tmem + lane_off + col + h * 32, v);
             tmem_wait_ld();
             const int row0 = (qb0 + it) * kBlockM + wg * 64 + h * 32;
@@ -335,6 +383,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int h = 0; h < D / 64; ++h) {
             float v[32];
+            if (!check_tmem(ck, tmem + lane_off + col + h * 32, 32, 32, __LINE__)) continue;
             tmem_ld32(tmem + lane_off + col + h * 32, v);
             tmem_wait_ld();
             if (qrow < NQ) {
@@ -361,6 +410,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
           float v[32];
+          if (!check_tmem(ck, tmem + lane_off + col + h * 32, 32, 32, __LINE__)) continue;
           tmem_ld32(tmem + lane_off + col + h * 32, v);
           tmem_wait_ld();
           if (key < NK) {
@@ -413,6 +463,15 @@ __global__ void streamkl_wait_selftest_kernel(int* dev_status, uint64_t timeout_
   __syncthreads();
 }
 
+// Runs one range check that must fail: a TMEM range past the 512 columns of
+// a (never made) allocation. Only the debug build records anything.
+__global__ void streamkl_check_selftest_kernel(int* dev_status) {
+  __shared__ int abort_flag;
+  abort_flag = 0;
+  const CheckCtx ck{0, 0, 0, 0, 0, 512, &abort_flag, dev_status};
+  check_tmem(ck, 500, 32, 32, __LINE__);
+}
+
 template <int D, bool GRAD1>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
   using L = BwdLayout<D, GRAD1>;
@@ -448,6 +507,11 @@ cudaError_t launch_dq_convert(const float* acc, void* out_bf16, long long n, cud
   if (blocks > 152LL * 16) blocks = 152LL * 16;
   streamkl_dq_convert_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
       reinterpret_cast<const float4*>(acc), static_cast<uint4*>(out_bf16), n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_check_selftest(int* dev_status, cudaStream_t stream) {
+  streamkl_check_selftest_kernel<<<1, 1, 0, stream>>>(dev_status);
   return cudaGetLastError();
 }
 

@@ -209,25 +209,42 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   // 64 entries each, so that a column pair's values are one 8-byte load
   float* tab = reinterpret_cast<float*>(gb + L::OFF_TAB);
 
+  // debug build: the layout's regions (TMEM fields are set once allocated)
+  CheckCtx ck{sb + L::OFF_X, sb + L::OFF_TAB, sb + L::OFF_BAR, sb + L::OFF_BAR + L::NBAR * 8, 0, 0,
+              abort_flag, dev_status};
   if (threadIdx.x == 0) {
-    mbar_init(x_full, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(y_full(s), 1);
-      mbar_init(y_empty(s), 1);
-    }
-    mbar_init(s_full, 1);
-    mbar_init(s_free, kSoftmaxWarps);   // one arrival per softmax warp
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(ds_full(b), kSoftmaxWarps);
-      mbar_init(ds_free(b), 1);
-    }
-    mbar_init(acc_full, 1);
-    mbar_init(drain, 2);  // one commit per MMA-issuing thread
-    mbar_init(x_free, 1);
-    mbar_init(acc_empty, kSoftmaxWarps);
     *abort_flag = 0;
-    // a failure recorded earlier (this launch or a previous one) skips the work
-    *skip_flag = *reinterpret_cast<volatile int*>(dev_status) != 0;
+    bool lay_ok = true;
+    if (kDeviceChecks) {  // every barrier address inside the barrier region
+      lay_ok = check_bar(ck, x_full, __LINE__) && check_bar(ck, s_full, __LINE__) &&
+               check_bar(ck, s_free, __LINE__) && check_bar(ck, acc_full, __LINE__) &&
+               check_bar(ck, drain, __LINE__) && check_bar(ck, x_free, __LINE__) &&
+               check_bar(ck, acc_empty, __LINE__);
+      for (int s = 0; s < kStages; ++s)
+        lay_ok = lay_ok && check_bar(ck, y_full(s), __LINE__) && check_bar(ck, y_empty(s), __LINE__);
+      for (int b = 0; b < 2; ++b)
+        lay_ok = lay_ok && check_bar(ck, ds_full(b), __LINE__) && check_bar(ck, ds_free(b), __LINE__);
+    }
+    if (lay_ok) {
+      mbar_init(x_full, 1);
+      for (int s = 0; s < kStages; ++s) {
+        mbar_init(y_full(s), 1);
+        mbar_init(y_empty(s), 1);
+      }
+      mbar_init(s_full, 1);
+      mbar_init(s_free, kSoftmaxWarps);   // one arrival per softmax warp
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(ds_full(b), kSoftmaxWarps);
+        mbar_init(ds_free(b), 1);
+      }
+      mbar_init(acc_full, 1);
+      mbar_init(drain, 2);  // one commit per MMA-issuing thread
+      mbar_init(x_free, 1);
+      mbar_init(acc_empty, kSoftmaxWarps);
+    }
+    // a failure recorded earlier (this launch or a previous one), or a
+    // failed layout check, skips the work
+    *skip_flag = !lay_ok || *reinterpret_cast<volatile int*>(dev_status) != 0;
     // malformed sequence offsets, or a causal sequence with more query rows
     // than keys: reported, never computed
     if (!I0.sv.ok || (causal && I0.nq > I0.nk)) atomicCAS(dev_status, 0, kStatusInvalidArg);
@@ -250,6 +267,12 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const bool skip = *skip_flag;
   const WaitCtx wc{abort_flag, dev_status, timeout_ns};
+  ck.tmem = tmem;
+  ck.tmem_cols = 512;
+  // TMA coordinate extents: rows of the X and Y maps, their third dimension
+  const int q_rows = PACKED ? total_q : NQ, k_rows = PACKED ? total_k : NK;
+  const int x_rows = DQ ? q_rows : k_rows, y_rows = DQ ? k_rows : q_rows;
+  const int z_hi = PACKED ? H : n_bh;
   // the items of this CTA in order; steps are numbered globally across them
   // (g = steps of the earlier items) for the Y ring and the per-step barriers
   auto item_steps = [&](const Item& I) { return skip ? 0 : I.n_iter; };
@@ -265,6 +288,13 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       if (lane == 0) {
         // persistent: the previous item's T GEMMs have read X
         if (ic > 0) ok = wait_bounded(x_free, (ic - 1) & 1, wc);
+        if (kDeviceChecks)
+          for (int t = 0; t < 2; ++t)
+            for (int b = 0; b < L::KB; ++b)
+              for (int h = 0; h < 2; ++h)
+                ok = ok && check_tma(ck, sb + L::OFF_X + t * L::XT + b * 16384 + h * 8192, 8192,
+                                     x_full, b * 64, D, I.x_row0 + I.x0 + h * kStepRows, x_rows,
+                                     kStepRows, I.sv.z, z_hi, __LINE__);
         if (ok) {
           mbar_arrive_expect_tx(x_full, 2 * L::XT);
 #pragma unroll
@@ -305,6 +335,14 @@ __global__ void __launch_bounds__(kSepThreads, 1)
           ts[2 * kStepRows + lane + 32] = c1.z, ts[3 * kStepRows + lane + 32] = -c1.w;
           __syncwarp();  // the arrive below publishes the whole warp's entries
         }
+        if (kDeviceChecks && lane == 0) {
+          const uint32_t dst = sb + L::OFF_Y + s * 2 * L::YT;
+          for (int t = 0; t < 2; ++t)
+            for (int b = 0; b < L::KB; ++b)
+              good = good && check_tma(ck, dst + t * L::YT + b * 8192, 8192, y_full(s), b * 64, D,
+                                       I.y_row0 + yrow, y_rows, kStepRows, I.sv.z, z_hi, __LINE__);
+        }
+        if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(y_full(s), 2 * L::YT);
           const uint32_t dst = sb + L::OFF_Y + s * 2 * L::YT;
@@ -368,7 +406,10 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         mma_commit(ds_free(G & 1));
         mma_commit(y_empty(G % kStages));
       };
-      bool ok = true;
+      // the T tiles, the two dS buffers and the accumulators inside the allocation
+      bool ok = check_tmem(ck, tmem + L::COL_T, 128, 128, __LINE__) &&
+                check_tmem(ck, tmem + L::COL_DS, 128, 128, __LINE__) &&
+                check_tmem(ck, tmem + L::COL_ACC, 128, L::NSETS * D, __LINE__);
       int g = 0, ic = 0;
       if (warp == 1) {
         // T of step G goes in as soon as the softmax warps have loaded T of
@@ -437,7 +478,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     for (int item = item_first; ok && item < n_items; item += item_stride) {
     const Item I = item == item_first ? I0 : item_at(item);
     const int n_iter = item_steps(I);
-    if (n_iter == 0 && !split_out) continue;
+    // an item without steps still runs its epilogue when no step reaches
+    // its X block at all (zero rows, below)
+    if (n_iter == 0 && !(I.active && I.n_iter == 0)) continue;
     const int xrow = I.x0 + r;
 
     // dQ kernel: constants of this thread's query row
@@ -457,6 +500,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       // and let the round trip overlap the T wait
       const bool tab = DQ || mbar_test_wait(y_full(G % kStages), (G / kStages) & 1);
       if (!__all_sync(0xffffffffu, wait_bounded(s_full, G & 1, wc))) return false;
+      if (!(check_tmem(ck, tmem + lane_off + L::COL_T + grp * 16, 32, 16, __LINE__) &&
+            check_tmem(ck, tmem + lane_off + L::COL_T + 64 + grp * 16, 32, 16, __LINE__)))
+        return false;
       tc_fence_after();
       tmem_ld16(tmem + lane_off + L::COL_T + grp * 16, a);
       tmem_ld16(tmem + lane_off + L::COL_T + 64 + grp * 16, b);
@@ -550,6 +596,10 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       // this thread's 16 values of row r: 8 packed columns per set at
       // [8 grp, 8 grp + 8) of the set's 32-column slot of buffer G&1
       const uint32_t dsb = tmem + lane_off + L::COL_DS + (G & 1) * 64 + grp * 8;
+      if (!check_tmem(ck, dsb, 32, (HAS2 && HAS1) ? 40 : 8, __LINE__)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();  // the stores below follow the MMAs that read this buffer
       if (HAS2) tmem_st8(dsb, d2p);
       if (HAS1) tmem_st8(dsb + (HAS2 ? 32 : 0), d1p);
@@ -565,16 +615,30 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     constexpr int EC = D / 4;
     auto part_row = [&](int t) {
       const size_t plane = static_cast<size_t>(gridDim.y) * NQ;
+      dcheck(ck, t < L::NSETS && static_cast<int>(blockIdx.z) < splits &&
+                     static_cast<size_t>(I.sv.v_off + xrow) < plane, __LINE__);
       return reinterpret_cast<float4*>(
           part + ((static_cast<size_t>(t) * splits + blockIdx.z) * plane +
                   static_cast<size_t>(I.sv.v_off + xrow)) * D + grp * EC);
     };
-    if (split_out && ok && I.active && n_iter == 0 && xrow < I.NX) {
+    // an X block no Y step reaches has zero gradient: a packed sequence
+    // without query rows (its keys' dK), or, with a key split, a split that
+    // holds no key of this query block (a zero partial)
+    if (ok && I.active && I.n_iter == 0 && xrow < I.NX) {
 #pragma unroll
       for (int t = 0; t < L::NSETS; ++t) {
-        float4* dst = part_row(t);
+        if (split_out) {
+          float4* dst = part_row(t);
 #pragma unroll
-        for (int i = 0; i < EC / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int i = 0; i < EC / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          __nv_bfloat16* out = (HAS2 && t == 0) ? out2 : out1;
+          uint4* dst = reinterpret_cast<uint4*>(
+              out + (DQ ? I.sv.q_off : I.sv.k_off) + static_cast<long long>(xrow) * I.sv.row_stride +
+              grp * EC);
+#pragma unroll
+          for (int i = 0; i < EC / 8; ++i) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
       }
     }
     if (ok && n_iter > 0 && __all_sync(0xffffffffu, wait_bounded(acc_full, ic & 1, wc))) {
@@ -583,6 +647,8 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       for (int t = 0; t < L::NSETS; ++t) {
         __nv_bfloat16* out = (HAS2 && t == 0) ? out2 : out1;
         float v[EC];
+        if (!check_tmem(ck, tmem + lane_off + L::COL_ACC + t * D + grp * EC, 32, EC, __LINE__))
+          break;
         if constexpr (EC == 32)
           tmem_ld32(tmem + lane_off + L::COL_ACC + t * D + grp * EC, v);
         else

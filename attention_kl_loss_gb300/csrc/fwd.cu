@@ -193,20 +193,34 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
   volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
 
+  // debug build: the layout's regions (TMEM fields are set once allocated)
+  CheckCtx ck{sb, sb + L::OFF_BAR, sb + L::OFF_BAR, sb + L::OFF_BAR + L::NBAR * 8, 0, 0,
+              abort_flag, dev_status};
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    for (int s = 0; s < L::STAGES; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
-    }
-    for (int k = 0; k < 2; ++k) {
-      mbar_init(s_full(k), 1);
-      mbar_init(s_empty(k), 4 * kGroups);  // one arrival per softmax warp
-    }
-    mbar_init(drain, 1);
     *abort_flag = 0;
-    // a failure recorded earlier (this launch or a previous one) skips the work
-    *skip_flag = *reinterpret_cast<volatile int*>(dev_status) != 0;
+    bool lay_ok = true;
+    if (kDeviceChecks) {  // every barrier address inside the barrier region
+      lay_ok = check_bar(ck, q_full, __LINE__) && check_bar(ck, drain, __LINE__);
+      for (int s = 0; s < L::STAGES; ++s)
+        lay_ok = lay_ok && check_bar(ck, kv_full(s), __LINE__) && check_bar(ck, kv_empty(s), __LINE__);
+      for (int k = 0; k < 2; ++k)
+        lay_ok = lay_ok && check_bar(ck, s_full(k), __LINE__) && check_bar(ck, s_empty(k), __LINE__);
+    }
+    if (lay_ok) {
+      mbar_init(q_full, 1);
+      for (int s = 0; s < L::STAGES; ++s) {
+        mbar_init(kv_full(s), 1);
+        mbar_init(kv_empty(s), 1);
+      }
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(s_full(k), 1);
+        mbar_init(s_empty(k), 4 * kGroups);  // one arrival per softmax warp
+      }
+      mbar_init(drain, 1);
+    }
+    // a failure recorded earlier (this launch or a previous one), or a
+    // failed layout check, skips the work
+    *skip_flag = !lay_ok || *reinterpret_cast<volatile int*>(dev_status) != 0;
     // malformed sequence offsets, or a causal sequence with more query rows
     // than keys (its first rows would see no key): reported, never computed
     if (!sv.ok || (causal && nq > nk)) atomicCAS(dev_status, 0, kStatusInvalidArg);
@@ -228,10 +242,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   if (*skip_flag) n_iter = 0;
   const WaitCtx wc{abort_flag, dev_status, timeout_ns};
+  ck.tmem = tmem;
+  ck.tmem_cols = 512;
+  // TMA coordinate extents: rows of the Q and K maps, their third dimension
+  const int q_rows = PACKED ? total_q : NQ, k_rows = PACKED ? total_k : NK;
+  const int z_hi = PACKED ? H : static_cast<int>(gridDim.z);
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_iter > 0) {
+    bool q_ok = true;
+    if (kDeviceChecks && lane == 0 && n_iter > 0)
+      for (int kb = 0; kb < L::KB; ++kb)
+        q_ok = q_ok &&
+               check_tma(ck, sb + L::OFF_Q1 + kb * 16384, 16384, q_full, kb * 64, D,
+                         sv.q_row0 + qb * kBlockM, q_rows, kBlockM, sv.z, z_hi, __LINE__) &&
+               check_tma(ck, sb + L::OFF_Q2 + kb * 16384, 16384, q_full, kb * 64, D,
+                         sv.q_row0 + qb * kBlockM, q_rows, kBlockM, sv.z, z_hi, __LINE__);
+    if (lane == 0 && n_iter > 0 && q_ok) {
       mbar_arrive_expect_tx(q_full, 2 * L::TILE);
 #pragma unroll
       for (int kb = 0; kb < L::KB; ++kb) {
@@ -245,9 +272,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         const int s = it % L::STAGES;
         const uint32_t ph = (it / L::STAGES) & 1;
         if (!wait_bounded(kv_empty(s), ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(kv_full(s), 2 * L::TILE);
         const int krow = sv.k_row0 + (t_begin + it) * kBlockN;
         const uint32_t dst = sb + L::OFF_K + s * 2 * L::TILE;
+        bool k_ok = true;
+        if (kDeviceChecks)
+          for (int kb = 0; kb < L::KB; ++kb)
+            k_ok = k_ok &&
+                   check_tma(ck, dst + kb * 16384, 16384, kv_full(s), kb * 64, D, krow, k_rows,
+                             kBlockN, sv.z, z_hi, __LINE__) &&
+                   check_tma(ck, dst + L::TILE + kb * 16384, 16384, kv_full(s), kb * 64, D, krow,
+                             k_rows, kBlockN, sv.z, z_hi, __LINE__);
+        if (!k_ok) break;
+        mbar_arrive_expect_tx(kv_full(s), 2 * L::TILE);
 #pragma unroll
         for (int kb = 0; kb < L::KB; ++kb) {
           tma_load_3d(dst + kb * 16384, &tm_k1, kv_full(s), kb * 64, krow, sv.z);
@@ -275,6 +311,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tc_fence_after();
         const uint32_t kbase = sb + L::OFF_K + s * 2 * L::TILE;
         const uint32_t d1 = tmem + slot * 256, d2 = d1 + 128;
+        if (!check_tmem(ck, d1, 128, 256, __LINE__)) break;
         // the two GEMMs' k-steps interleaved: independent accumulators keep
         // the tensor pipe busy where one dependent chain would stall it
 #pragma unroll
@@ -308,6 +345,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       tc_fence_after();
       float a[32], b[32];
       const uint32_t ta = lane_base + slot * 256;
+      if (!(check_tmem(ck, ta, 32, 32, __LINE__) && check_tmem(ck, ta + 128, 32, 32, __LINE__)))
+        break;
       tmem_ld32(ta, a);
       tmem_ld32(ta + 128, b);
       tmem_wait_ld();
@@ -341,7 +380,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       }
       if (active && qrow < nq) {
         const size_t o = static_cast<size_t>(sv.v_off + static_cast<long long>(qrow) * sv.v_stride);
-        if (SPLIT) {
+        // (the debug build skips an out-of-range row's writes)
+        if (!dcheck(ck, o < static_cast<size_t>(plane), __LINE__)) {
+        } else if (SPLIT) {
           const size_t base = static_cast<size_t>(split) * plane + o;
           const size_t fstride = static_cast<size_t>(splits) * plane;
           part[0 * fstride + base] = st.r1;

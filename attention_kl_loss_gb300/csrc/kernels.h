@@ -62,8 +62,9 @@ __device__ __forceinline__ SeqView seq_view_packed(int bh, int H, int max_q, int
   v.q_off = (static_cast<long long>(q0) * H + h) * d;
   v.k_off = (static_cast<long long>(k0) * H + h) * d;
   v.row_stride = static_cast<long long>(H) * d;
+  // query rows need at least one key (a softmax over no key is undefined)
   v.ok = q0 >= 0 && k0 >= 0 && v.nq >= 0 && v.nk >= 0 && v.nq <= max_q && v.nk <= max_k &&
-         q1 <= total_q && k1 <= total_k;
+         q1 <= total_q && k1 <= total_k && !(v.nq > 0 && v.nk == 0);
   return v;
 }
 
@@ -138,16 +139,45 @@ struct BwdSepArgs {
   uint64_t timeout_ns;
 };
 
+// Fused backward for short query sweeps (N_Q <= 64, d = 128, dense batches):
+// a persistent grid over (batch-head, 128-key tile) items; dK written per
+// item, dQ kept in TMEM per batch-head and added to the fp32 accumulators
+// (zeroed by the caller) when a CTA's batch-head changes.
+struct BwdShortArgs {
+  const CUtensorMap* tm_q1;  // 64-column x 64-row boxes
+  const CUtensorMap* tm_k1;
+  const CUtensorMap* tm_q2;
+  const CUtensorMap* tm_k2;
+  int BH, NQ, NK, causal;
+  int grad1, grad2;  // gradient sets: configuration 2 (dQ1/dK1), configuration 1 (dQ2/dK2)
+  float scale;
+  const float* kl;
+  const float* lse1;
+  const float* lse2;
+  const float* g;
+  void* dk2;       // bf16 [BH][NK][d]
+  void* dk1;
+  float* dq2acc;   // fp32 [BH][NQ][d]
+  float* dq1acc;
+  int ctas;        // persistent grid size (one CTA per SM)
+  int* dev_status;
+  uint64_t timeout_ns;
+};
+constexpr int kShortMaxQ = 64;  // query rows the short-sweep kernel handles
+
 // Each returns the launch error (cudaSuccess when queued).
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_fwd_combine(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_separate(const BwdSepArgs& a, cudaStream_t stream);
+cudaError_t launch_bwd_short(const BwdShortArgs& a, cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* acc, void* out_bf16, long long n, cudaStream_t stream);
 cudaError_t launch_wait_selftest(int* dev_status, uint64_t timeout_ns, cudaStream_t stream);
+cudaError_t launch_check_selftest(int* dev_status, cudaStream_t stream);
 
 size_t fwd_smem_bytes(int d);
 size_t bwd_smem_bytes(int d, int grad1);
 size_t bwd_sep_smem_bytes(int d, int grad1);
+size_t bwd_short_smem_bytes(int grad1, int grad2);
 
 }  // namespace skl

@@ -9,13 +9,23 @@
 #pragma once
 
 #include <cstdint>
+#include <cstdio>
 #include <cuda.h>
 #include <cuda_bf16.h>
 
 namespace skl {
 
-constexpr int kStatusInvalidArg = 1;  // == STREAMKL_ERR_INVALID_ARG
-constexpr int kStatusTimeout = 4;     // == STREAMKL_ERR_TIMEOUT
+constexpr int kStatusInvalidArg = 1;   // == STREAMKL_ERR_INVALID_ARG
+constexpr int kStatusTimeout = 4;      // == STREAMKL_ERR_TIMEOUT
+constexpr int kStatusDeviceCheck = 5;  // == STREAMKL_ERR_DEVICE_CHECK
+
+// Device-side range checks, compiled in only when STREAMKL_DEVICE_CHECKS is
+// defined (the library's debug build).
+#ifdef STREAMKL_DEVICE_CHECKS
+constexpr bool kDeviceChecks = true;
+#else
+constexpr bool kDeviceChecks = false;
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -91,6 +101,76 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
       return false;
     }
   }
+}
+
+// ---------------------------------------------------------------- debug checks
+// The debug build checks the operands of every TMA copy, TMEM access and
+// mbarrier operation against the kernel's layout before it is issued. A
+// failed check raises the CTA's abort flag (every bounded wait then gives
+// up and the roles drain and exit as after a timeout), records
+// STREAMKL_ERR_DEVICE_CHECK in the caller's status word unless a failure was
+// recorded first, prints the source line once per launch and returns false,
+// so that the caller skips the access. Nothing traps. In the release build
+// every check is the constant true and its operands are never computed.
+struct CheckCtx {
+  uint32_t data_lo, data_hi;  // shared-memory bytes TMA copies may write
+  uint32_t bar_lo, bar_hi;    // the mbarrier region
+  uint32_t tmem;              // TMEM base address of the CTA's allocation
+  uint32_t tmem_cols;         // columns allocated
+  volatile int* abort_flag;
+  int* dev_status;
+};
+
+static __device__ __noinline__ void device_check_failed(const CheckCtx& k, int line) {
+  *k.abort_flag = 1;
+  if (atomicCAS(k.dev_status, 0, kStatusDeviceCheck) == 0)
+    printf("streamkl: device check failed at line %d (block %d,%d,%d thread %d)\n", line,
+           static_cast<int>(blockIdx.x), static_cast<int>(blockIdx.y),
+           static_cast<int>(blockIdx.z), static_cast<int>(threadIdx.x));
+}
+
+__device__ __forceinline__ bool dcheck(const CheckCtx& k, bool ok, int line) {
+  if constexpr (kDeviceChecks) {
+    if (!ok) device_check_failed(k, line);
+    return ok;
+  } else {
+    return true;
+  }
+}
+
+// An mbarrier inside the barrier region, on its 8-byte boundary.
+__device__ __forceinline__ bool check_bar(const CheckCtx& k, uint32_t bar, int line) {
+  return dcheck(k, bar >= k.bar_lo && bar + 8 <= k.bar_hi && (bar & 7u) == 0, line);
+}
+
+// A TMA tile load of `bytes` into `dst`, completing on `bar`: destination in
+// the data region on a 1024-byte boundary (the 128-byte swizzle repeats every
+// 1024 bytes); inner coordinate a multiple of 8 elements (16 bytes of bf16)
+// inside [0, c0_hi); row coordinate inside [0, c1_hi + box rows) (a tile may
+// start past a ragged end, where it reads zeros); third coordinate inside
+// [0, c2_hi).
+__device__ __forceinline__ bool check_tma(const CheckCtx& k, uint32_t dst, uint32_t bytes,
+                                          uint32_t bar, int c0, int c0_hi, int c1, int c1_hi,
+                                          int box_rows, int c2, int c2_hi, int line) {
+  return dcheck(k,
+                dst >= k.data_lo && dst + bytes <= k.data_hi && (dst & 1023u) == 0 &&
+                    bar >= k.bar_lo && bar + 8 <= k.bar_hi && (bar & 7u) == 0 && c0 >= 0 &&
+                    c0 < c0_hi && (c0 & 7) == 0 && c1 >= 0 && c1 < c1_hi + box_rows && c2 >= 0 &&
+                    c2 < c2_hi,
+                line);
+}
+
+// A TMEM access at taddr (lane << 16 | column) covering `lanes` lanes and
+// `cols` columns: a warp-wide access (lanes = 32) starts on its 32-lane
+// quarter; the columns stay inside the allocation.
+__device__ __forceinline__ bool check_tmem(const CheckCtx& k, uint32_t taddr, int lanes, int cols,
+                                           int line) {
+  const uint32_t lane = taddr >> 16, lane0 = k.tmem >> 16;
+  const int col = static_cast<int>(taddr & 0xFFFFu) - static_cast<int>(k.tmem & 0xFFFFu);
+  return dcheck(k,
+                lane >= lane0 && lane - lane0 + lanes <= 128 && ((lane - lane0) & 31u) == 0 &&
+                    col >= 0 && col + cols <= static_cast<int>(k.tmem_cols),
+                line);
 }
 
 // Drain wait used on the way out: same bound, but never raises a status

@@ -25,7 +25,9 @@
  *   STREAMKL_ERR_UNSUPPORTED before anything is enqueued; a failed launch
  *   returns STREAMKL_ERR_CUDA. streamkl_last_error() gives the detail.
  * - dev_status is a caller-owned device int the kernels write when a bounded
- *   wait inside them gives up (STREAMKL_ERR_TIMEOUT); they never clear it.
+ *   wait inside them gives up (STREAMKL_ERR_TIMEOUT), when packed sequence
+ *   offsets are malformed (STREAMKL_ERR_INVALID_ARG) or, in the debug build,
+ *   when a range check fails (STREAMKL_ERR_DEVICE_CHECK); they never clear it.
  *   Clear it before use and read it after synchronising the stream. Results
  *   of a call that set it are undefined.
  */
@@ -43,7 +45,13 @@ typedef enum {
   STREAMKL_ERR_INVALID_ARG = 1,
   STREAMKL_ERR_UNSUPPORTED = 2,
   STREAMKL_ERR_CUDA = 3,
-  STREAMKL_ERR_TIMEOUT = 4
+  STREAMKL_ERR_TIMEOUT = 4,
+  /* Written to dev_status only by the debug build (libstreamkl_debug.so,
+   * compiled with STREAMKL_DEVICE_CHECKS): a kernel found an operand of a
+   * TMA copy, TMEM access or mbarrier outside its layout, skipped that access
+   * and stopped (the first failing source line is printed from the device).
+   * The release build never writes it. */
+  STREAMKL_ERR_DEVICE_CHECK = 5
 } streamkl_status;
 
 /* Human-readable name of a status code (static string). */
@@ -262,8 +270,10 @@ streamkl_status streamkl_bwd_reverse(const void* q1, const void* k1, const void*
  * No split-K and no workspace. Host-side errors as for streamkl_fwd; the
  * offsets live on the device, so the kernels check them and write
  * STREAMKL_ERR_INVALID_ARG into *dev_status for offsets outside [0, total],
- * a length above its max_seqlen, or a causal sequence with more query rows
- * than keys (its rows of that sequence are then left unwritten).
+ * a length above its max_seqlen, a sequence with query rows but no key (a
+ * softmax over no key is undefined), or a causal sequence with more query
+ * rows than keys (its rows of that sequence are then left unwritten). A
+ * sequence without query rows contributes nothing.
  */
 streamkl_status streamkl_fwd_varlen(const void* q1, const void* k1, const void* q2, const void* k2,
                                     const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
@@ -277,7 +287,8 @@ streamkl_status streamkl_fwd_varlen(const void* q1, const void* k1, const void* 
  * [total_q, H]; gradients bf16 [total_q, H, d] (dq2, dq1) and [total_k, H, d]
  * (dk2, dk1), either pair NULL to skip that configuration (at least one
  * pair). Always the separate dK/dQ kernels; no workspace. Errors as for
- * streamkl_bwd and streamkl_fwd_varlen.
+ * streamkl_bwd and streamkl_fwd_varlen. The dK rows of a sequence without
+ * query rows are zero (no query sees those keys).
  */
 streamkl_status streamkl_bwd_varlen(const void* q1, const void* k1, const void* q2, const void* k2,
                                     const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
@@ -296,6 +307,17 @@ streamkl_status streamkl_bwd_varlen(const void* q1, const void* k1, const void* 
  */
 streamkl_status streamkl_selftest_wait_timeout(int* dev_status, unsigned timeout_us,
                                                void* stream);
+
+/*
+ * Self-test of the debug build's range checks: launches one tiny kernel that
+ * checks a TMEM column range lying past any allocation (no TMEM is allocated
+ * and nothing is accessed). In the debug build (libstreamkl_debug.so) the
+ * check fails and records STREAMKL_ERR_DEVICE_CHECK in *dev_status; in the
+ * release build the checks are compiled out and *dev_status is left as it
+ * was. The paper has no counterpart; it exists so that the report path of
+ * the checks can be tested without a faulty access.
+ */
+streamkl_status streamkl_selftest_device_check(int* dev_status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -55,10 +55,19 @@ def _check(status, where):
 
 
 def sweep_algo(reps: int):
-    """Fused (dQ through fp32 L2 reductions) against separate dK/dQ kernels."""
+    """The fused algorithm (at most 64 query rows at d = 128: the short-sweep
+    kernel with dQ kept on chip per batch-head; otherwise one CTA per key tile
+    with dQ through fp32 L2 reductions) against the separate dK/dQ kernels."""
     dev = torch.device("cuda")
     shapes = [synthetic.WORKLOADS[n] for n in ("mid", "stress", "splitk", "causal64k")] + [
         synthetic.custom("decode64", B=4, H=32, NQ=64, NK=65536, d=128, causal=True, noise=0.1),
+        synthetic.custom("decode64_both", B=4, H=32, NQ=64, NK=65536, d=128, causal=True,
+                         noise=0.1, grad1=True),
+        synthetic.custom("decode1", B=4, H=32, NQ=1, NK=65536, d=128, causal=True, noise=0.1),
+        synthetic.custom("decode16_128k", B=4, H=32, NQ=16, NK=131072, d=128, causal=True,
+                         noise=0.1),
+        synthetic.custom("decode32_nc", B=1, H=32, NQ=32, NK=32768, d=128, causal=False,
+                         noise=0.1),
         synthetic.custom("square16k_d64", B=1, H=16, NQ=16384, NK=16384, d=64, causal=True,
                          noise=0.2, grad1=True),
         synthetic.custom("square8k", B=2, H=16, NQ=8192, NK=8192, d=128, causal=False, noise=0.2,

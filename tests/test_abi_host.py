@@ -38,8 +38,57 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     for code, name in enumerate(["OK", "ERR_INVALID_ARG", "ERR_UNSUPPORTED", "ERR_CUDA",
-                                 "ERR_TIMEOUT"]):
+                                 "ERR_TIMEOUT", "ERR_DEVICE_CHECK"]):
         assert lib.streamkl_status_string(code).decode() == "STREAMKL_" + name
+
+
+def test_status_codes_agree_across_header_binding_and_kernels():
+    """The device-side status codes (ptx.cuh), the header's enum and the
+    binding's constants name the same numbers."""
+    from attention_kl_loss_gb300 import binding
+    text = open(HEADER).read()
+    enum = dict((n, int(v)) for n, v in re.findall(r"(STREAMKL_\w+)\s*=\s*(\d+)", text))
+    for name in ("STREAMKL_ERR_INVALID_ARG", "STREAMKL_ERR_TIMEOUT", "STREAMKL_ERR_DEVICE_CHECK"):
+        assert enum[name] == getattr(binding, name)
+    ptx = open(os.path.join(ROOT, "attention_kl_loss_gb300", "csrc", "ptx.cuh")).read()
+    dev = dict((n, int(v)) for n, v in re.findall(r"constexpr int (kStatus\w+) = (\d+);", ptx))
+    assert dev == {"kStatusInvalidArg": enum["STREAMKL_ERR_INVALID_ARG"],
+                   "kStatusTimeout": enum["STREAMKL_ERR_TIMEOUT"],
+                   "kStatusDeviceCheck": enum["STREAMKL_ERR_DEVICE_CHECK"]}
+
+
+def test_device_status_is_raised_with_its_name():
+    """raise_on_device_status turns each device code into a named error (CPU
+    tensor: the synchronise is skipped on a host tensor)."""
+    import torch
+    from attention_kl_loss_gb300 import binding
+    orig = torch.cuda.synchronize
+    try:
+        torch.cuda.synchronize = lambda *a, **k: None
+        for code, name in [(4, "TIMEOUT"), (5, "DEVICE_CHECK"), (1, "INVALID_ARG")]:
+            with pytest.raises(binding.StreamKLError) as e:
+                binding.raise_on_device_status(torch.tensor([code], dtype=torch.int32), "test")
+            assert e.value.status == code and f"STREAMKL_ERR_{name}" in str(e.value)
+        binding.raise_on_device_status(torch.tensor([0], dtype=torch.int32), "test")
+    finally:
+        torch.cuda.synchronize = orig
+
+
+def test_debug_build_exports_every_declared_symbol():
+    """The debug build (device-side range checks) builds from the same sources
+    and exports the same entry points; the binding can route its calls to it."""
+    from attention_kl_loss_gb300 import binding, build
+    path = build.build(debug=True)
+    assert path.endswith("libstreamkl_debug.so") and os.path.exists(path)
+    dbg = binding.load(debug=True)
+    for name in declared_functions():
+        assert hasattr(dbg, name), name
+    assert dbg.streamkl_status_string(5).decode() == "STREAMKL_ERR_DEVICE_CHECK"
+    rel = binding.load(debug=False)
+    assert dbg is not rel
+    with binding.use_debug_library() as lib:
+        assert lib is dbg and binding.load() is dbg
+    assert binding.load() is rel
 
 
 def test_split_choice(lib):
@@ -88,11 +137,15 @@ def test_workspace_sizes(lib):
 
 def test_automatic_backward_choice(lib):
     lib.streamkl_set_bwd_algorithm(-1)
-    # separate kernels on every shape unless forced
-    for args in [(1, 32, 65536, 65536, 128, 1, 1), (4, 32, 64, 65536, 128, 1, 0),
+    # separate kernels unless the query rows fit the fused short-sweep kernel
+    # (at most 64 at d = 128)
+    for args in [(1, 32, 65536, 65536, 128, 1, 1), (4, 32, 65, 65536, 128, 1, 0),
                  (4, 32, 512, 131072, 128, 1, 0), (4, 32, 256, 65536, 128, 1, 0),
-                 (4, 32, 512, 131072, 64, 1, 0)]:
+                 (4, 32, 512, 131072, 64, 1, 0), (4, 32, 64, 65536, 64, 1, 0)]:
         assert lib.streamkl_bwd_algorithm(*args) == 0, args
+    for args in [(4, 32, 64, 65536, 128, 1, 0), (1, 8, 1, 4096, 128, 0, 1),
+                 (2, 2, 17, 300, 128, 1, 1)]:
+        assert lib.streamkl_bwd_algorithm(*args) == 1, args
 
 
 def test_dq_key_split_choice(lib):

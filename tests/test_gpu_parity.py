@@ -276,23 +276,31 @@ def test_persistent_dk_kernel(NQ, NK, d, causal, sets, ctas):
                     assert_grad(host(got[i][b, hh]), og[i], name)
 
 
-def test_decode_shape_automatic_paths():
+@pytest.mark.parametrize("algo", ALGOS)
+def test_decode_shape_automatic_paths(algo):
     """A decode-like shape (64 query rows against 8K keys, 4 slices) with both
-    gradient sets through the reverse entry points and the library's own
-    choices, which here are the persistent dK kernel and a dQ key split;
-    against the oracle's definition with the distributions in that order."""
+    gradient sets through the reverse entry points: the separate algorithm
+    with its own choices for this shape (the persistent dK kernel and a dQ
+    key split), and the fused algorithm, which here is the short-sweep
+    kernel; against the oracle's definition with the distributions in that
+    order."""
     w = synthetic.custom("decode_auto", B=2, H=2, NQ=64, NK=8192, d=128, causal=True, noise=0.4,
                          grad1=True)
     assert binding.bwd_dk_persist(w.B, w.H, w.NQ, w.NK, w.d, w.causal) > 0
     assert binding.bwd_dq_splits(w.B, w.H, w.NQ, w.NK, w.d, w.causal, True) > 1
+    assert binding.bwd_algorithm(w.B, w.H, w.NQ, w.NK, w.d, w.causal, True) == binding.BWD_FUSED
     dev = torch.device("cuda")
     ins = synthetic.make_inputs(w, 23, dev)
     q1, k1, q2, k2, g = ins
     status = binding.new_status(dev)
     kl, lse1, lse2 = binding.streamkl_fwd_reverse(q1, k1, q2, k2, w.scale, w.causal,
                                                   dev_status=status)
-    grads = binding.streamkl_bwd_reverse(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
-                                         grad1=True, dev_status=status)
+    binding.set_bwd_algorithm(algo)
+    try:
+        grads = binding.streamkl_bwd_reverse(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                             grad1=True, dev_status=status)
+    finally:
+        binding.set_bwd_algorithm(None)
     binding.raise_on_device_status(status, "decode shape")
     for b in range(w.B):
         for hh in range(w.H):
@@ -305,6 +313,45 @@ def test_decode_shape_automatic_paths():
             for got, ref, name in ((grads[0], s_dq, "student dq2"), (grads[1], s_dk, "student dk2"),
                                    (grads[2], t_dq, "teacher dq1"), (grads[3], t_dk, "teacher dk1")):
                 assert_grad(host(got[b, hh]), ref, name)
+
+
+SHORT = [
+    # (B, H, N_Q, N_K, causal, sets): decode-like shapes for the fused short-sweep
+    # kernel; 40 slices x 8 key tiles = 320 items on 152 CTAs put several
+    # batch-heads (segments, each flushing its dQ) on one CTA
+    (1, 2, 1, 1000, True, "both"),
+    (2, 3, 64, 4096 + 77, True, "both"),
+    (1, 4, 17, 3000, False, "both"),
+    (2, 2, 33, 200, True, "config1"),
+    (4, 10, 20, 1000, True, "both"),
+    (4, 10, 64, 1000, False, "config1"),
+]
+
+
+@pytest.mark.parametrize("B,H,NQ,NK,causal,sets", SHORT)
+def test_short_sweep_fused_backward(B, H, NQ, NK, causal, sets):
+    """The fused algorithm's short-sweep kernel (at most 64 query rows, d =
+    128: one visit per (query, key) pair, dQ kept on chip per batch-head)
+    against the oracle, slice by slice, and the library choosing it."""
+    w = synthetic.custom(f"short_{B}x{H}x{NQ}x{NK}", B=B, H=H, NQ=NQ, NK=NK, d=128, causal=causal,
+                         noise=0.4, grad1=sets == "both")
+    assert binding.bwd_algorithm(B, H, NQ, NK, 128, causal, w.grad1) == binding.BWD_FUSED
+    dev = torch.device("cuda")
+    q1, k1, q2, k2, _ = synthetic.make_inputs(w, 29, dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(30)
+    g = torch.randn((B, H, NQ), generator=gen, device=dev, dtype=torch.float32)
+    ins, outs, grads = run(w, inputs=(q1, k1, q2, k2, g))
+    for b in range(B):
+        for hh in range(H):
+            h = [host(t[b, hh]) for t in ins[:4]]
+            og = orc.head_backward(*h, w.scale, w.causal, g[b, hh].cpu().numpy().astype(np.float64),
+                                   w.grad1)
+            for i, name in enumerate(["dq2", "dk2", "dq1", "dk1"]):
+                if og[i] is None:
+                    assert grads[i] is None
+                    continue
+                assert_grad(host(grads[i][b, hh]), og[i], f"{name} slice {b},{hh}")
 
 
 @pytest.mark.parametrize("algo", ALGOS)

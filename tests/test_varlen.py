@@ -47,6 +47,9 @@ def test_packed_batch_matches_oracle_per_sequence(d, causal):
     for b in range(len(lens_q)):
         qs, qe, ks, ke = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
         if qe == qs:
+            # no query sees this sequence's keys: their gradients are exactly 0
+            for t in (grads[1], grads[3]):
+                assert torch.all(t[ks:ke].float() == 0), b
             continue
         for h in range(2):
             sl = [_f64(t[a:e, h]) for t, a, e in ((q1, qs, qe), (k1, ks, ke), (q2, qs, qe),
@@ -84,4 +87,18 @@ def test_device_checks_of_the_offsets():
     the status word (the kernels return normally; what they computed is not
     to be used)."""
     _, _, _, st = _run([50, 200], [80, 100], 2, 64, True, seed=3)
+    assert int(st.item()) == binding.STREAMKL_ERR_INVALID_ARG
+
+
+def test_sequence_with_queries_but_no_keys_is_reported():
+    """Query rows with no key at all (non-causal) have no softmax: the forward
+    reports STREAMKL_ERR_INVALID_ARG through the status word."""
+    dev = torch.device("cuda")
+    lens_q, lens_k = [40, 30], [0, 90]
+    q1, k1, q2, k2, g, cu_q, cu_k = synthetic.make_packed_inputs(lens_q, lens_k, 2, 64, 4,
+                                                                 device=dev)
+    st = binding.new_status(dev)
+    binding.streamkl_fwd_varlen(q1, k1, q2, k2, cu_q, cu_k, max(lens_q), max(lens_k), None, False,
+                                dev_status=st)
+    torch.cuda.synchronize()
     assert int(st.item()) == binding.STREAMKL_ERR_INVALID_ARG
