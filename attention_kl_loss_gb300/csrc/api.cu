@@ -194,22 +194,33 @@ size_t bwd_ws(int B, int H, int NQ, int NK, int d, int grad1) {
 // Key split of the separate backward's dQ kernel. Like the forward's key
 // split (gist.science technical summary, section 3 "Variante Split-K") it fills the GPU
 // when there are few query blocks: each split sweeps a contiguous range of
-// 64-key steps into an fp32 partial dQ, and a combine kernel sums the
+// key steps into an fp32 partial dQ, and a combine kernel sums the
 // partials. Same wave model as the forward's choice, with the dQ kernel's
-// per-step cost (~1 us at d = 128) and the partials' extra bytes.
+// per-step cost (~1 us per 64 keys at d = 128, 0.6 us at d = 64; a 128-key
+// step of the one-set d = 64 kernel ~1.6 times a 64-key one) and the
+// partials' extra bytes.
 std::atomic<int> g_forced_dq_splits{0};  // 0: automatic
 
-int dq_steps(int NK) { return (NK + 63) / 64; }
+// Key rows per step of the separate backward's dQ kernel: 128 with one
+// gradient set at d = 64, 64 otherwise (the kernel's layout).
+int sep_step_rows(int nsets, int d) { return (nsets == 1 && d == 64) ? 128 : 64; }
+
+int dq_steps(int NK, int nsets, int d) {
+  const int step = sep_step_rows(nsets, d);
+  return (NK + step - 1) / step;
+}
 
 int dq_splits_auto(int B, int H, int NQ, int NK, int d, int nsets) {
   const long long ctas = static_cast<long long>((NQ + skl::kBlockM - 1) / skl::kBlockM) * B * H;
-  const int steps = dq_steps(NK);
+  const int steps = dq_steps(NK, nsets, d);
   const int sms = num_sms();
   if (ctas >= 8LL * sms) return 1;
-  const double step_us = d == 128 ? 1.0 : 0.6, cta_us = 4.0;
+  const double step_us = (d == 128 ? 1.0 : 0.6) * (sep_step_rows(nsets, d) == 128 ? 1.6 : 1.0);
+  const double cta_us = 4.0;
   const double in_bytes = static_cast<double>(B) * H * (static_cast<double>(NK) + NQ) * d * 4.0;
   const double part_bytes = static_cast<double>(B) * H * NQ * d * 4.0 * nsets;
-  const int smax = std::max(1, std::min(32, steps / 8));
+  // at least 512 keys per split
+  const int smax = std::max(1, std::min(32, steps * sep_step_rows(nsets, d) / 512));
   auto cost = [&](int s) {
     const long long units = ctas * s;
     const long long waves = (units + sms - 1) / sms;
@@ -237,7 +248,7 @@ int dq_splits_auto(int B, int H, int NQ, int NK, int d, int nsets) {
 // Effective split count and key steps per split (dense batches).
 void dq_split_plan(int B, int H, int NQ, int NK, int d, int nsets, int* splits, int* per) {
   const int forced = g_forced_dq_splits.load();
-  const int steps = dq_steps(NK);
+  const int steps = dq_steps(NK, nsets, d);
   const int req = forced > 0 ? forced : dq_splits_auto(B, H, NQ, NK, d, nsets);
   const int s = std::max(1, std::min(req, steps));
   *per = (steps + s - 1) / s;

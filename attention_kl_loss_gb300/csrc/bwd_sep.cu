@@ -5,23 +5,26 @@
 // and the saved LSEs, P_t = exp(S_t - LSE_t).
 //
 // One template serves both kernels. A CTA keeps 128 rows of a "stationary"
-// tensor pair X1, X2 in shared memory and streams 64-row steps of the other
-// pair Y1, Y2 through a ring of 4-8 stages:
+// tensor pair X1, X2 in shared memory and streams steps of STEP rows of the
+// other pair Y1, Y2 through a ring of 4-8 stages (STEP = 64; 128 in the dQ
+// kernel with one gradient set at d = 64):
 //   dQ kernel: X = Q (query block), Y = K steps;  acc_t += dS_t   K_t
 //   dK kernel: X = K (key block),   Y = Q steps;  acc_t += dS_t^T Q_t
-// In both, T_t = X_t Y_t^T (M = 128 X rows, N = 64 Y rows) is the score tile
-// seen from the X side (S_t in the dQ kernel, S_t^T in the dK kernel), the
-// softmax warps turn T1, T2 into the matching dS tiles and the gradient GEMM
-// is acc_t += dT_t Y_t (M = 128, N = d, K = 64), accumulated in TMEM over the
-// whole sweep and written out once. With few query blocks the dQ kernel
+// In both, T_t = X_t Y_t^T (M = 128 X rows, N = STEP Y rows) is the score
+// tile seen from the X side (S_t in the dQ kernel, S_t^T in the dK kernel),
+// the softmax warps turn T1, T2 into the matching dS tiles and the gradient
+// GEMM is acc_t += dT_t Y_t (M = 128, N = d, K = STEP), accumulated in TMEM
+// over the whole sweep and written out once. With few query blocks the dQ kernel
 // also splits its keys across CTAs (grid z): each split writes its
 // accumulator as an fp32 partial and a combine kernel sums the partials.
 //
 // dS never goes through shared memory: each softmax thread owns one X row,
 // which is one TMEM lane, so it stores its bf16 dS values straight into TMEM
-// and the gradient GEMMs read their A operand from there. TMEM columns:
-//   T [0,128) (T1 low 64, T2 high 64) | dS buffer 0 [128,192) | dS buffer 1
-//   [192,256) (set 2 low 32, set 1 high 32) | acc set 2 [256, 256+d) | acc set 1
+// and the gradient GEMMs read their A operand from there. TMEM columns (64-row
+// steps): T [0,128) (T1 low 64, T2 high 64) | dS buffer 0 [128,192) | dS
+// buffer 1 [192,256) (set 2 low 32, set 1 high 32) | acc set 2 [256, 256+d) |
+// acc set 1; 128-row steps (one set): T1, T2 128 each | two 64-column dS
+// buffers | acc.
 // Shared memory holds only X (64 KB at d = 128), the Y ring and, in the dK
 // kernel, a per-stage table of per-query constants. The T GEMMs of step j+1
 // are issued as soon as the softmax warps have loaded T of step j, and run
@@ -42,7 +45,7 @@
 // constant table of each Y stage (all lanes); 1 = TMEM owner + T-GEMM issuer;
 // 18 = gradient-GEMM issuer; 2..17 = softmax and epilogue. Warp w reads TMEM lanes [32 (w%4), +32) (its
 // quarter) and serves column group g = (w-2)/4: thread = X row (TMEM lane),
-// owning Y columns [16g, 16g+16) of every step and, at the end, d columns
+// owning Y columns [g STEP/4, (g+1) STEP/4) of every step and, at the end, d columns
 // [g d/4, (g+1) d/4) of its output row. Per-query constants (LSE1, LSE2, g,
 // KL) are per row in the dQ kernel (registers) and per column in the dK kernel
 // (the table, written next to each Y stage and published by its barrier).
@@ -56,7 +59,7 @@ namespace {
 constexpr int kSepThreads = 608;  // 19 warps
 constexpr int kGradWarp = 18;     // issues the gradient GEMMs
 constexpr int kSoftmaxWarps = 16;
-constexpr int kStepRows = 64;     // Y rows per step
+constexpr int kBoxRows = 64;      // rows of one TMA box
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Gradient sets a launch computes (bit mask): configuration 1 (P1 fixed)
@@ -67,14 +70,25 @@ template <int D, bool DQ, int SETS>
 struct SepLayout {
   static constexpr int KB = D / 64;                   // 128-byte boxes per row
   static constexpr int XT = kBlockM * D * 2;          // 128 rows of one X tensor
-  static constexpr int YT = kStepRows * D * 2;        // 64 rows of one Y tensor
   static constexpr int NSETS = SETS == (kSet1 | kSet2) ? 2 : 1;
+  // Y rows per step: 128 in the dQ kernel with one gradient set at d = 64
+  // (T1, T2 at N = 128, where the T GEMMs run at the tensor pipe's full rate
+  // against two thirds of it at N = 64, and two dS buffers fit TMEM next to
+  // one accumulator; five 32 KB Y stages fit shared memory); 64 otherwise:
+  // two accumulators leave TMEM room for N = 64 only, the dK kernel's
+  // per-column constants and 32 columns per thread spill its registers, and
+  // at d = 128 only two 64 KB stages fit, which exposes the tile loads
+  // (measured: mid and split-K backward 14-17 % slower than with 64-row steps)
+  static constexpr int STEP = (NSETS == 1 && DQ && D == 64) ? 128 : 64;
+  static constexpr int YT = STEP * D * 2;             // one Y tensor of a step
+  static constexpr int YBOX = STEP * 128;             // one 64-column box of it
+  static constexpr int NCOL = STEP / 4;               // Y columns per softmax thread
   // as many Y stages as fit next to X (and the dK kernel's tables)
-  static constexpr int STAGES = D == 64 ? 8 : (DQ ? 5 : 4);
+  static constexpr int STAGES = STEP == 128 ? (D == 64 ? 5 : 2) : (D == 64 ? 8 : (DQ ? 5 : 4));
   static constexpr int OFF_X = 0;                     // X1, X2
   static constexpr int OFF_Y = 2 * XT;                // stage s: Y1 at +2s YT, Y2 at +(2s+1) YT
-  static constexpr int OFF_TAB = OFF_Y + STAGES * 2 * YT;  // dK: [stage][4][64] float
-  static constexpr int TAB_BYTES = DQ ? 0 : STAGES * 4 * kStepRows * 4;
+  static constexpr int OFF_TAB = OFF_Y + STAGES * 2 * YT;  // dK: [stage][4][STEP] float
+  static constexpr int TAB_BYTES = DQ ? 0 : STAGES * 4 * STEP * 4;
   static constexpr int OFF_BAR = OFF_TAB + TAB_BYTES;
   // x_full, y_full[S], y_empty[S], s_full, s_free, ds_full[2], ds_free[2],
   // acc_full, drain, x_free, acc_empty (the last two: persistent kernel)
@@ -82,7 +96,10 @@ struct SepLayout {
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;
-  static constexpr uint32_t COL_T = 0, COL_DS = 128, COL_ACC = 256;
+  // TMEM: T1 [0, STEP), T2 [STEP, 2 STEP) | dS buffers 0, 1 (DSW columns
+  // each: STEP/2 packed columns per set) | accumulators (D columns per set)
+  static constexpr uint32_t COL_T = 0, COL_DS = 2 * STEP, DSW = NSETS * STEP / 2;
+  static constexpr uint32_t COL_ACC = COL_DS + 2 * DSW;
   static_assert(COL_ACC + NSETS * D <= 512, "TMEM budget");
   static_assert(ALLOC <= 232448, "shared memory budget");
 };
@@ -153,14 +170,14 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     I.x0 = xb * kBlockM;
     I.x_row0 = DQ ? I.sv.q_row0 : I.sv.k_row0;
     I.y_row0 = DQ ? I.sv.k_row0 : I.sv.q_row0;
-    int y_end;  // in steps of 64 Y rows
+    int y_end;  // in steps of STEP Y rows
     if (DQ) {  // key steps visible to some row of this query block
       const int klim = causal ? min(I.nk, min(I.nq, I.x0 + kBlockM) + I.off) : I.nk;
       I.y_begin = 0;
-      y_end = (klim + kStepRows - 1) / kStepRows;
+      y_end = (klim + L::STEP - 1) / L::STEP;
     } else {  // query steps with a row that sees some key of this block
-      I.y_begin = causal ? max(0, I.x0 - I.off) / kStepRows : 0;
-      y_end = (I.nq + kStepRows - 1) / kStepRows;
+      I.y_begin = causal ? max(0, I.x0 - I.off) / L::STEP : 0;
+      y_end = (I.nq + L::STEP - 1) / L::STEP;
     }
     // dQ kernel with a key split: this CTA takes key steps [z S, z S + S) of
     // them (S = split_steps, z = blockIdx.z) and writes an fp32 partial dQ
@@ -293,8 +310,8 @@ __global__ void __launch_bounds__(kSepThreads, 1)
             for (int b = 0; b < L::KB; ++b)
               for (int h = 0; h < 2; ++h)
                 ok = ok && check_tma(ck, sb + L::OFF_X + t * L::XT + b * 16384 + h * 8192, 8192,
-                                     x_full, b * 64, D, I.x_row0 + I.x0 + h * kStepRows, x_rows,
-                                     kStepRows, I.sv.z, z_hi, __LINE__);
+                                     x_full, b * 64, D, I.x_row0 + I.x0 + h * kBoxRows, x_rows,
+                                     kBoxRows, I.sv.z, z_hi, __LINE__);
         if (ok) {
           mbar_arrive_expect_tx(x_full, 2 * L::XT);
 #pragma unroll
@@ -305,7 +322,7 @@ __global__ void __launch_bounds__(kSepThreads, 1)
               for (int h = 0; h < 2; ++h)
                 tma_load_3d(sb + L::OFF_X + t * L::XT + b * 16384 + h * 8192,
                             t == 0 ? &tm_x1 : &tm_x2, x_full, b * 64,
-                            I.x_row0 + I.x0 + h * kStepRows, I.sv.z);
+                            I.x_row0 + I.x0 + h * kBoxRows, I.sv.z);
           ++n_x;
         }
       }
@@ -317,41 +334,51 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       for (; it < n; ++it) {
         const int G = g + it;
         const int s = G % kStages;
-        const int yrow = (I.y_begin + it) * kStepRows;
-        float4 c0, c1;  // dK kernel: this lane's two table entries, loaded before the wait
+        const int yrow = (I.y_begin + it) * L::STEP;
+        // dK kernel: this lane's table entries (rows yrow + lane + 32 e),
+        // loaded before the wait
+        constexpr int NE = L::STEP / 32;
+        float4 ce[NE];
         if (!DQ) {
-          c0 = query_const(lse1_in, lse2_in, g_in, kl_in, qv(yrow + lane), scale, yrow + lane < I.nq);
-          c1 = query_const(lse1_in, lse2_in, g_in, kl_in, qv(yrow + lane + 32), scale,
-                           yrow + lane + 32 < I.nq);
+#pragma unroll
+          for (int e = 0; e < NE; ++e)
+            ce[e] = query_const(lse1_in, lse2_in, g_in, kl_in, qv(yrow + lane + 32 * e), scale,
+                                yrow + lane + 32 * e < I.nq);
         }
         bool good = true;
         if (lane == 0) good = wait_bounded(y_empty(s), ((G / kStages) & 1) ^ 1, wc);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (!DQ) {
-          float* ts = tab + s * 4 * kStepRows;
-          ts[lane] = -c0.x, ts[kStepRows + lane] = -c0.y;
-          ts[2 * kStepRows + lane] = c0.z, ts[3 * kStepRows + lane] = -c0.w;
-          ts[lane + 32] = -c1.x, ts[kStepRows + lane + 32] = -c1.y;
-          ts[2 * kStepRows + lane + 32] = c1.z, ts[3 * kStepRows + lane + 32] = -c1.w;
+          float* ts = tab + s * 4 * L::STEP;
+#pragma unroll
+          for (int e = 0; e < NE; ++e) {
+            const int j = lane + 32 * e;
+            ts[j] = -ce[e].x, ts[L::STEP + j] = -ce[e].y;
+            ts[2 * L::STEP + j] = ce[e].z, ts[3 * L::STEP + j] = -ce[e].w;
+          }
           __syncwarp();  // the arrive below publishes the whole warp's entries
         }
-        if (kDeviceChecks && lane == 0) {
-          const uint32_t dst = sb + L::OFF_Y + s * 2 * L::YT;
+        // a step's Y tile: per tensor, 64-column boxes of STEP rows, each
+        // loaded as 64-row TMA boxes
+        const uint32_t dst = sb + L::OFF_Y + s * 2 * L::YT;
+        if (kDeviceChecks && lane == 0)
           for (int t = 0; t < 2; ++t)
             for (int b = 0; b < L::KB; ++b)
-              good = good && check_tma(ck, dst + t * L::YT + b * 8192, 8192, y_full(s), b * 64, D,
-                                       I.y_row0 + yrow, y_rows, kStepRows, I.sv.z, z_hi, __LINE__);
-        }
+              for (int h = 0; h < L::STEP / kBoxRows; ++h)
+                good = good && check_tma(ck, dst + t * L::YT + b * L::YBOX + h * 8192, 8192, y_full(s),
+                                         b * 64, D, I.y_row0 + yrow + h * kBoxRows, y_rows, kBoxRows,
+                                         I.sv.z, z_hi, __LINE__);
         if (!__shfl_sync(0xffffffffu, good, 0)) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(y_full(s), 2 * L::YT);
-          const uint32_t dst = sb + L::OFF_Y + s * 2 * L::YT;
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
             for (int b = 0; b < L::KB; ++b)
-              tma_load_3d(dst + t * L::YT + b * 8192, t == 0 ? &tm_y1 : &tm_y2, y_full(s), b * 64,
-                          I.y_row0 + yrow, I.sv.z);
+#pragma unroll
+              for (int h = 0; h < L::STEP / kBoxRows; ++h)
+                tma_load_3d(dst + t * L::YT + b * L::YBOX + h * 8192, t == 0 ? &tm_y1 : &tm_y2,
+                            y_full(s), b * 64, I.y_row0 + yrow + h * kBoxRows, I.sv.z);
         }
       }
       g += it;
@@ -370,7 +397,7 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     // overlap the other's MMAs in the tensor pipe. A thread's commit tracks
     // only the MMAs that thread issued.
     if (lane == 0 && (PERSIST || item_steps(I0) > 0)) {
-      constexpr uint32_t id_t = idesc_bf16(kBlockM, kStepRows, 0, 0);
+      constexpr uint32_t id_t = idesc_bf16(kBlockM, L::STEP, 0, 0);
       constexpr uint32_t id_g = idesc_bf16(kBlockM, D, 0, 1);
       const uint32_t x1 = sb + L::OFF_X, x2 = x1 + L::XT;
       // Descriptors are built once per stage and advanced by compile-time
@@ -381,10 +408,10 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         const uint64_t dy = smem_desc_sw128(sb + L::OFF_Y + (G % kStages) * 2 * L::YT, 16, 1024);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t xo = (k >> 2) * 16384 + (k & 3) * 32, yo = (k >> 2) * 8192 + (k & 3) * 32;
+          const uint32_t xo = (k >> 2) * 16384 + (k & 3) * 32, yo = (k >> 2) * L::YBOX + (k & 3) * 32;
           mma_bf16(tmem + L::COL_T, desc_advance(dx1, xo), desc_advance(dy, yo), id_t, k > 0);
-          mma_bf16(tmem + L::COL_T + 64, desc_advance(dx2, xo), desc_advance(dy, L::YT + yo), id_t,
-                   k > 0);
+          mma_bf16(tmem + L::COL_T + L::STEP, desc_advance(dx2, xo), desc_advance(dy, L::YT + yo),
+                   id_t, k > 0);
         }
         mma_commit(s_full);
       };
@@ -393,22 +420,22 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       // set's Y (set 2: Y2, set 1: Y1) MN-major; with two sets their k-steps
       // interleave; the item's first step starts the accumulators
       auto issue_g = [&](int G, int j) {
-        const uint64_t dy = smem_desc_sw128(sb + L::OFF_Y + (G % kStages) * 2 * L::YT, 8192, 1024);
-        const uint32_t dsb = tmem + L::COL_DS + (G & 1) * 64;
+        const uint64_t dy = smem_desc_sw128(sb + L::OFF_Y + (G % kStages) * 2 * L::YT, L::YBOX, 1024);
+        const uint32_t dsb = tmem + L::COL_DS + (G & 1) * L::DSW;
 #pragma unroll
-        for (int kg = 0; kg < 4; ++kg)
+        for (int kg = 0; kg < L::STEP / 16; ++kg)
 #pragma unroll
           for (int t = 0; t < L::NSETS; ++t) {
             const bool set2 = HAS2 && t == 0;
-            mma_bf16_ts(tmem + L::COL_ACC + t * D, dsb + 32 * t + 8 * kg,
+            mma_bf16_ts(tmem + L::COL_ACC + t * D, dsb + (L::STEP / 2) * t + 8 * kg,
                         desc_advance(dy, (set2 ? L::YT : 0) + kg * 2048), id_g, (j > 0 || kg > 0));
           }
         mma_commit(ds_free(G & 1));
         mma_commit(y_empty(G % kStages));
       };
       // the T tiles, the two dS buffers and the accumulators inside the allocation
-      bool ok = check_tmem(ck, tmem + L::COL_T, 128, 128, __LINE__) &&
-                check_tmem(ck, tmem + L::COL_DS, 128, 128, __LINE__) &&
+      bool ok = check_tmem(ck, tmem + L::COL_T, 128, 2 * L::STEP, __LINE__) &&
+                check_tmem(ck, tmem + L::COL_DS, 128, 2 * L::DSW, __LINE__) &&
                 check_tmem(ck, tmem + L::COL_ACC, 128, L::NSETS * D, __LINE__);
       int g = 0, ic = 0;
       if (warp == 1) {
@@ -438,8 +465,11 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         // softmax warps' critical path, these GEMMs are not (their dS buffer is
         // next written two steps on). The dQ kernel, bound by the tensor pipe,
         // lags by 2; the dK kernel, whose shallower Y ring must be released
-        // sooner, by 1.
-        constexpr int kGradLag = DQ ? 2 : 1;
+        // sooner, by 1. The lag stays below the ring's depth: the T GEMMs of
+        // step G + lag need the Y stage that step G's gradient GEMMs release
+        // once the ring has wrapped.
+        constexpr int kGradLag = (DQ && kStages >= 3) ? 2 : 1;
+        static_assert(kGradLag < kStages, "gradient GEMM lag below the Y ring's depth");
         for (int item = item_first; ok && item < n_items; item += item_stride) {
           const Item I = item == item_first ? I0 : item_at(item);
           const int n = item_steps(I);
@@ -493,19 +523,25 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     // T of global step G into a, b (all lanes agree on every wait's outcome,
     // so the warp-wide TMEM loads and the __syncwarp below are never reached
     // by part of a warp); then the T GEMMs of step G+1 may overwrite T
-    float a[16], b[16];
+    constexpr int NC = L::NCOL;  // this thread's Y columns per step
+    float a[NC], b[NC];
     auto load_t = [&](int G) {
       // dK kernel: the stage's barrier also publishes its constant table; its
       // phase completed before these T GEMMs were issued, so test it first
       // and let the round trip overlap the T wait
       const bool tab = DQ || mbar_test_wait(y_full(G % kStages), (G / kStages) & 1);
       if (!__all_sync(0xffffffffu, wait_bounded(s_full, G & 1, wc))) return false;
-      if (!(check_tmem(ck, tmem + lane_off + L::COL_T + grp * 16, 32, 16, __LINE__) &&
-            check_tmem(ck, tmem + lane_off + L::COL_T + 64 + grp * 16, 32, 16, __LINE__)))
+      const uint32_t ta = tmem + lane_off + L::COL_T + grp * NC;
+      if (!(check_tmem(ck, ta, 32, NC, __LINE__) && check_tmem(ck, ta + L::STEP, 32, NC, __LINE__)))
         return false;
       tc_fence_after();
-      tmem_ld16(tmem + lane_off + L::COL_T + grp * 16, a);
-      tmem_ld16(tmem + lane_off + L::COL_T + 64 + grp * 16, b);
+      if constexpr (NC == 32) {
+        tmem_ld32(ta, a);
+        tmem_ld32(ta + L::STEP, b);
+      } else {
+        tmem_ld16(ta, a);
+        tmem_ld16(ta + L::STEP, b);
+      }
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
@@ -522,29 +558,29 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         break;
       }
       const int G = g + it;
-      const int y0 = (I.y_begin + it) * kStepRows + grp * 16;  // first Y row of this thread's columns
+      const int y0 = (I.y_begin + it) * L::STEP + grp * NC;  // first Y row of this thread's columns
       // the gradient GEMMs of step G-2 have read this step's dS buffer: nearly
       // always done by now; test early, block only if not
       const bool ds_ready = mbar_test_wait(ds_free(G & 1), ((G >> 1) & 1) ^ 1);
-      uint32_t d2p[8], d1p[8];
+      uint32_t d2p[NC / 2], d1p[NC / 2];
       {
-        // visibility of (query, key) over this thread's 16 columns
+        // visibility of (query, key) over this thread's NC columns
         bool full;
         int lim = 0;
         if (DQ) {
           lim = causal ? min(I.nk, xrow + 1 + I.off) : I.nk;  // keys < lim visible
-          full = y0 + 16 <= lim;
+          full = y0 + NC <= lim;
         } else {
           lim = causal ? xrow - I.off : 0;  // queries >= lim (and < N_Q) see this key
-          full = y0 + 16 <= I.nq && y0 >= lim;
+          full = y0 + NC <= I.nq && y0 >= lim;
         }
         auto visible = [&](int y) { return DQ ? y < lim : (y < I.nq && y >= lim); };
-        const float* tq = tab + (G % kStages) * 4 * kStepRows + grp * 16;
+        const float* tq = tab + (G % kStages) * 4 * L::STEP + grp * NC;
         const float2 c2 = make_float2(c, c), sc2 = make_float2(scale, scale);
         const float2 m1 = make_float2(-1.f, -1.f);
         float4 q1c, q2c, qgc, qec;  // dK kernel: 4 columns of each constant, one 16-byte load each
 #pragma unroll
-        for (int k = 0; k < 16; k += 2) {
+        for (int k = 0; k < NC; k += 2) {
           float2 nb1, nb2, gs, ne;
           if (DQ) {
             nb1 = make_float2(-rc.x, -rc.x);
@@ -554,9 +590,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
           } else {
             if ((k & 3) == 0) {
               q1c = *reinterpret_cast<const float4*>(tq + k);
-              q2c = *reinterpret_cast<const float4*>(tq + kStepRows + k);
-              qgc = *reinterpret_cast<const float4*>(tq + 2 * kStepRows + k);
-              if (HAS1) qec = *reinterpret_cast<const float4*>(tq + 3 * kStepRows + k);
+              q2c = *reinterpret_cast<const float4*>(tq + L::STEP + k);
+              qgc = *reinterpret_cast<const float4*>(tq + 2 * L::STEP + k);
+              if (HAS1) qec = *reinterpret_cast<const float4*>(tq + 3 * L::STEP + k);
             }
             const bool lo = (k & 3) == 0;
             nb1 = lo ? make_float2(q1c.x, q1c.y) : make_float2(q1c.z, q1c.w);
@@ -587,26 +623,31 @@ __global__ void __launch_bounds__(kSepThreads, 1)
           }
         }
       }
-      if (it + 1 < n_iter) good = load_t(G + 1);
+      // 64-row steps: load the next T before storing this dS (the next T GEMMs
+      // start earlier); 128-row steps store first, which keeps this step's
+      // packed dS out of the registers the next T lands in
+      constexpr bool kLoadFirst = L::STEP == 64;
+      if (kLoadFirst && it + 1 < n_iter) good = load_t(G + 1);
       if (!__all_sync(0xffffffffu, ds_ready) &&
           !__all_sync(0xffffffffu, wait_bounded(ds_free(G & 1), ((G >> 1) & 1) ^ 1, wc))) {
         ok = false;
         break;
       }
-      // this thread's 16 values of row r: 8 packed columns per set at
-      // [8 grp, 8 grp + 8) of the set's 32-column slot of buffer G&1
-      const uint32_t dsb = tmem + lane_off + L::COL_DS + (G & 1) * 64 + grp * 8;
-      if (!check_tmem(ck, dsb, 32, (HAS2 && HAS1) ? 40 : 8, __LINE__)) {
+      // this thread's NC values of row r: NC/2 packed columns per set at
+      // [NC/2 grp, NC/2 (grp + 1)) of the set's STEP/2-column slot of buffer G&1
+      const uint32_t dsb = tmem + lane_off + L::COL_DS + (G & 1) * L::DSW + grp * (NC / 2);
+      if (!check_tmem(ck, dsb, 32, (HAS2 && HAS1) ? L::STEP / 2 + NC / 2 : NC / 2, __LINE__)) {
         ok = false;
         break;
       }
       tc_fence_after();  // the stores below follow the MMAs that read this buffer
-      if (HAS2) tmem_st8(dsb, d2p);
-      if (HAS1) tmem_st8(dsb + (HAS2 ? 32 : 0), d1p);
+      if (HAS2) tmem_st_cols<NC / 2>(dsb, d2p);
+      if (HAS1) tmem_st_cols<NC / 2>(dsb + (HAS2 ? L::STEP / 2 : 0), d1p);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full(G & 1));
+      if (!kLoadFirst && it + 1 < n_iter) good = load_t(G + 1);
     }
     // epilogue: accumulator row r -> bf16 dQ (dQ kernel) or dK (dK kernel)
     // row, d columns [grp d/4, (grp+1) d/4); with a key split, the fp32 row

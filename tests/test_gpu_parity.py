@@ -210,7 +210,8 @@ def test_dq_key_split(NQ, NK, d, causal, sets, splits):
     binding.set_bwd_algorithm(binding.BWD_SEPARATE)
     binding.set_bwd_dq_splits(splits)
     try:
-        steps = (NK + 63) // 64  # 64-key steps; each split takes ceil(steps / splits)
+        step = 128 if (sets != "both" and d == 64) else 64  # key rows per step of the dQ kernel
+        steps = (NK + step - 1) // step  # each split takes ceil(steps / splits)
         per = -(-steps // min(splits, steps))
         assert binding.bwd_dq_splits(w.B, w.H, NQ, NK, d, causal, sets == "both") == -(-steps // per)
         grads = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
