@@ -76,6 +76,9 @@ WORKLOADS = {
         # the split-K shape on 4 of its 32 heads (keys 1.07 GB, above L2):
         # DRAM-traffic captures of the split forward
         Workload("splitk_h4", B=4, H=4, NQ=512, NK=131072, d=128, causal=True, noise=0.1),
+        # a decode-like shape (64 query rows against 64K keys) on 8 heads, for
+        # profiler captures of the fused short-sweep backward (keys 268 MB)
+        Workload("decode_profile", B=1, H=8, NQ=64, NK=65536, d=128, causal=True, noise=0.1),
     ]
 }
 

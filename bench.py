@@ -544,9 +544,15 @@ def gpu_arm(args, w):
         bwd_note = ("separate dK and dQ kernels, timed together (one API call); each "
                     "regenerates S1 and S2, so they execute 16d FLOPs per pair with both "
                     "gradient sets against the method's 12d")
+    elif NQ <= 64 and d == 128:
+        bwd_name = "streamkl_bwd_kernel"
+        bwd_note = ("fused algorithm, short-sweep kernel (streamkl_bwd_short_kernel: each pair "
+                    "visited once, dQ kept on chip per batch-head); includes the workspace clear "
+                    "and the fp32->bf16 dQ conversion; bound by HBM")
     else:
         bwd_name = "streamkl_bwd_kernel"
         bwd_note = "fused kernel; includes the workspace clear and the fp32->bf16 dQ conversion"
+    short_sweep = (not separate) and NQ <= 64 and d == 128
     step_flops = f_fwd + f_bwd_metric
     value = world * step_flops / (ms_step * 1e-3) / 1e12
     pk = peaks()
@@ -576,7 +582,18 @@ def gpu_arm(args, w):
                 "algorithmic": unit_note,
                 "peak_source": f"{pk['source']} bf16_tflops_sustained (kernel timed inside a long step)",
                 "frac_of_measured_burst": dom_tf / burst}
-    if dom == bwd_name:
+    if dom == bwd_name and short_sweep:
+        # the short-sweep backward moves the keys once and writes dK: HBM-bound
+        mb = bwd_min_bytes(w)
+        gbs = mb / (bwd_ms * 1e-3) / 1e9
+        roofline.update({"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / pk["hbm_gbs"],
+                         "algorithmic": "minimum bytes of the backward: Q1, K1, Q2, K2 read once, "
+                                        "the gradients written once, the per-row vectors read",
+                         "peak_source": f"{pk['source']} hbm_gbs (copy bandwidth)",
+                         "tensor_tflops": bwd_tf})
+        roofline.pop("frac_of_measured_burst", None)
+    elif dom == bwd_name:
         roofline["executed_tflops"] = bwd_xtf
         roofline["executed_frac"] = bwd_xtf / sustained
         if traffic is not None:

@@ -188,22 +188,21 @@ def sweep_dkpersist(reps: int):
 
 def sweep_configs(reps: int):
     """Forward and backward of every named workload at the library's choices,
-    with the exact visible-pair FLOP counts: 4d per pair forward; the
-    separate backward executes 12d per pair with one gradient set (each of
-    its two kernels recomputes both score tiles, 4d, and runs one gradient
-    GEMM, 2d) and 16d with both."""
+    with the exact visible-pair FLOP counts of the method's work: 4d per pair
+    forward; backward 4d to regenerate S1, S2 plus 4d per gradient set (8d
+    with one set, 12d with both). The separate backward executes 4d more
+    (each of its two kernels regenerates both score tiles)."""
     import json
-    import os
     dev = torch.device("cuda")
     peak = None
-    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
-                        "MEASURED_PEAKS.json")
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             peak = json.load(f).get("bf16_tflops_sustained")
-    print("| workload | sets | fwd ms | bwd ms | fwd TFLOP/s | bwd TFLOP/s executed | "
-          f"fwd / bwd of {'measured sustained peak' if peak else 'peak (not available)'} |")
-    print("|---|---|---:|---:|---:|---:|---|")
+    print("| workload | sets | bwd algorithm | fwd ms | bwd ms | fwd TFLOP/s | bwd TFLOP/s method "
+          "(executed) | fwd / bwd method of "
+          f"{'measured sustained peak' if peak else 'peak (not available)'} |")
+    print("|---|---|---|---:|---:|---:|---:|---|")
     for name in ("tiny", "mid", "causal64k", "splitk", "stress"):
         w = synthetic.WORKLOADS[name]
         (q1, k1, q2, k2, g), st = _setup(w, dev)
@@ -215,11 +214,14 @@ def sweep_configs(reps: int):
                                                 grad1=w.grad1, dev_status=st), reps)
         _check(st, name)
         pairs = w.live_pairs_per_head() * w.B * w.H
+        sep = binding.bwd_algorithm(w.B, w.H, w.NQ, w.NK, w.d, w.causal, w.grad1) == binding.BWD_SEPARATE
         ff = 4 * w.d * pairs / tf / 1e9
-        fb = (16 if w.grad1 else 12) * w.d * pairs / tb / 1e9
-        frac = f"{ff / peak:.2f} / {fb / peak:.2f}" if peak else "-"
+        fm = (12 if w.grad1 else 8) * w.d * pairs / tb / 1e9
+        fx = fm + (4 * w.d * pairs / tb / 1e9 if sep else 0.0)
+        frac = f"{ff / peak:.2f} / {fm / peak:.2f}" if peak else "-"
         print(f"| {name} (B{w.B} H{w.H} {w.NQ}x{w.NK} d{w.d}{' causal' if w.causal else ''}) | "
-              f"{'both' if w.grad1 else 'config 1'} | {tf:.3f} | {tb:.3f} | {ff:.0f} | {fb:.0f} | {frac} |")
+              f"{'both' if w.grad1 else 'config 1'} | {'separate' if sep else 'fused'} | {tf:.3f} | "
+              f"{tb:.3f} | {ff:.0f} | {fm:.0f} ({fx:.0f}) | {frac} |")
         del q1, k1, q2, k2, g
         torch.cuda.empty_cache()
 
