@@ -62,6 +62,8 @@ def parse_args(argv=None):
     p.add_argument("--cpu-budget-s", type=float, default=15.0,
                    help="target CPU seconds for the oracle sample")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--e2e-groups", type=int, default=4,
+                   help="(batch, head) groups a step's batch is streamed in for the e2e leg")
     p.add_argument("--no-configs", action="store_true",
                    help="skip the per-workload entries (times and oracle errors)")
     return p.parse_args(argv)
@@ -693,7 +695,7 @@ def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
     host_in = [t.cpu().pin_memory() for t in (q1, k1, q2, k2, g)]
     del q1, k1, q2, k2, g
     bh = w.B * w.H
-    groups = next(c for c in (4, 2, 1) if bh % c == 0)
+    groups = next(c for c in (args.e2e_groups, 4, 2, 1) if c >= 1 and bh % c == 0)
     per = bh // groups
 
     def part(t, i):  # slices [i per, (i+1) per) of the flattened (batch, head) axis, as [1, per, ...]
