@@ -53,6 +53,8 @@ _SIGNATURES = {
                                   _P, _P, _P, _P, _Z, _P, _P]),
     "streamkl_selftest_wait_timeout": (_I, [_P, ctypes.c_uint, _P]),
     "streamkl_selftest_device_check": (_I, [_P, _P]),
+    "streamkl_fwd_pairs": (_I, [_I, _I, _I, _I, _I, _I, _I]),
+    "streamkl_set_fwd_pairs": (_I, [_I]),
     "streamkl_bwd_algorithm": (_I, [_I, _I, _I, _I, _I, _I, _I]),
     "streamkl_set_bwd_algorithm": (_I, [_I]),
     "streamkl_bwd_dq_splits": (_I, [_I, _I, _I, _I, _I, _I, _I]),
@@ -190,6 +192,17 @@ def set_bwd_dk_persist(ctas: Optional[int]) -> None:
     """Force the persistent dK kernel (n CTAs), turn it off (-1), or None/0: automatic."""
     if load().streamkl_set_bwd_dk_persist(0 if ctas is None else int(ctas)) != 0:
         raise ValueError(f"invalid persistent dK CTA count {ctas!r}")
+
+
+def fwd_pairs(B, H, NQ, NK, d, causal, num_splits=0) -> bool:
+    """Whether streamkl_fwd runs as CTA pairs (cta_group::2) for these sizes."""
+    return int(load().streamkl_fwd_pairs(B, H, NQ, NK, d, int(causal), int(num_splits))) == 1
+
+
+def set_fwd_pairs(enabled: Optional[bool]) -> None:
+    """Use CTA pairs in the forward where the sizes allow (True), or not
+    (False / None: the default), for this process."""
+    load().streamkl_set_fwd_pairs(1 if enabled else 0)
 
 
 def set_bwd_algorithm(algo: Optional[int]) -> None:

@@ -132,6 +132,17 @@ int choose_splits_impl(int B, int H, int NQ, int NK, int d) {
   return best;
 }
 
+// Forward as CTA pairs (cta_group::2 MMAs over two query blocks), for dense
+// batches without a key split and with an even number of query blocks, when
+// switched on (streamkl_set_fwd_pairs(1)). Off by default: measured on
+// GB300 it matches the one-CTA kernel at 64K causal (27.6 against 28.0 ms)
+// and is 3-8 % slower on the smaller workloads.
+std::atomic<int> g_fwd_pairs{0};  // 0: never, 1: when eligible
+
+bool fwd_pairs_impl(int NQ, int splits) {
+  return g_fwd_pairs.load() == 1 && skl::fwd_pair_eligible(NQ, splits, false);
+}
+
 // Effective split count and tiles per split for a requested count.
 void split_plan(int requested, int NK, int* splits, int* tps) {
   const int tiles = key_tiles(NK);
@@ -412,6 +423,22 @@ int streamkl_set_bwd_dq_splits(int splits) {
   return 0;
 }
 
+int streamkl_fwd_pairs(int B, int H, int NQ, int NK, int d, int causal, int num_splits) {
+  if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK || num_splits < 0) return -1;
+  int s, tps;
+  split_plan(num_splits > 0 ? num_splits : choose_splits_impl(B, H, NQ, NK, d), NK, &s, &tps);
+  return fwd_pairs_impl(NQ, s) ? 1 : 0;
+}
+
+int streamkl_set_fwd_pairs(int mode) {
+  if (mode != 0 && mode != 1) {
+    fail(STREAMKL_ERR_INVALID_ARG, "mode must be 0 (never, the default) or 1 (when eligible)");
+    return -1;
+  }
+  g_fwd_pairs.store(mode);
+  return 0;
+}
+
 int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
   if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return -1;
   return bwd_algo_impl(B, H, NQ, NK, d, want_grad1 ? 1 : 0);
@@ -452,13 +479,17 @@ streamkl_status streamkl_fwd(const void* q1, const void* k1, const void* q2, con
     return fail(STREAMKL_ERR_INVALID_ARG, "forward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
 
   const int BH = B * H;
+  // CTA pairs: each CTA loads 64-row halves of the key tiles
+  const bool pairs = fwd_pairs_impl(NQ, splits);
+  const int k_box = pairs ? 64 : skl::kBlockM;
   CUtensorMap mq1, mk1, mq2, mk2;
   if ((st = make_map(&mq1, q1, BH, NQ, d, "q1")) != STREAMKL_OK) return st;
-  if ((st = make_map(&mk1, k1, BH, NK, d, "k1")) != STREAMKL_OK) return st;
+  if ((st = make_map(&mk1, k1, BH, NK, d, "k1", k_box)) != STREAMKL_OK) return st;
   if ((st = make_map(&mq2, q2, BH, NQ, d, "q2")) != STREAMKL_OK) return st;
-  if ((st = make_map(&mk2, k2, BH, NK, d, "k2")) != STREAMKL_OK) return st;
+  if ((st = make_map(&mk2, k2, BH, NK, d, "k2", k_box)) != STREAMKL_OK) return st;
 
   skl::FwdArgs a{};
+  a.pairs = pairs;
   a.tm_q1 = &mq1;
   a.tm_k1 = &mk1;
   a.tm_q2 = &mq2;

@@ -409,6 +409,295 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// The same forward as CTA pairs (dense batches, no split, an even number of
+// query blocks). A cluster of two CTAs takes two query blocks of one
+// (batch, head) slice and runs S1, S2 as tcgen05 MMAs with M = 256 over both
+// (cta_group::2): each CTA keeps its own Q tile and loads only half of every
+// key tile (64 keys), and the MMAs read the other half from the peer's shared
+// memory. Per CTA that halves the key bytes loaded and the B-operand bytes
+// the MMAs read, the shared-memory traffic the single-CTA kernel's MMAs are
+// bound by. The even CTA issues the MMAs; the odd CTA's warp 1 relays the
+// arrival of its Q tile and key halves to the even CTA's barriers; both
+// CTAs' softmax warps free an S buffer on the even CTA's barrier; the even
+// CTA's commits arrive on both CTAs' barriers. Each CTA reads its own rows of
+// S from its own TMEM, so the softmax / KL part is the single-CTA kernel's.
+// The pair sweeps the key tiles of its later query block; the earlier block
+// masks the keys past its frontier.
+template <int D>
+struct PairLayout {
+  static constexpr int KB = D / 64;
+  static constexpr int TILE = kBlockM * D * 2;     // one 128-row Q tile
+  static constexpr int HALF = 64 * D * 2;          // 64 rows of one K tensor
+  static constexpr int STAGES = D == 128 ? 4 : 8;
+  static constexpr int OFF_Q1 = 0;
+  static constexpr int OFF_Q2 = TILE;
+  static constexpr int OFF_K = 2 * TILE;           // stage s: K1 half at +2s HALF, K2 half at +(2s+1) HALF
+  static constexpr int OFF_BAR = OFF_K + STAGES * 2 * HALF;
+  // q_full, q_peer, kv_full[S], kv_peer[S], kv_empty[S], s_full[2], s_empty[2], drain
+  static constexpr int NBAR = 2 + 3 * STAGES + 4 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr int OFF_XCH = OFF_MISC + 16;
+  static constexpr int BYTES = OFF_XCH + (kGroups - 1) * 5 * kBlockM * 4;
+  static constexpr int ALLOC = BYTES + 1024;
+  static_assert(ALLOC <= 232448, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kFwdThreads, 1)
+    streamkl_fwd_pair_kernel(const __grid_constant__ CUtensorMap tm_q1,
+                             const __grid_constant__ CUtensorMap tm_k1,
+                             const __grid_constant__ CUtensorMap tm_q2,
+                             const __grid_constant__ CUtensorMap tm_k2, int NQ, int NK, int causal,
+                             float scale, float* __restrict__ kl_out, float* __restrict__ lse1_out,
+                             float* __restrict__ lse2_out, int* dev_status, uint64_t timeout_ns) {
+  using L = PairLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sb = (raw + 1023u) & ~1023u;
+  uint8_t* gb = smem_raw + (sb - raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+  const int bh = static_cast<int>(blockIdx.z);
+  const int nqb = (NQ + kBlockM - 1) / kBlockM;  // even
+  const int pair = static_cast<int>(blockIdx.x) >> 1;
+  // causal: heavy pairs first; the even CTA takes the later block of the pair
+  const int qb_hi = causal ? nqb - 1 - 2 * pair : 2 * pair + 1;
+  const int qb = rank == 0 ? qb_hi : qb_hi - 1;
+  const int off = NK - NQ;
+  const int klim_pair = causal ? min(NK, min(NQ, (qb_hi + 1) * kBlockM) + off) : NK;
+  int n_iter = (klim_pair + kBlockN - 1) / kBlockN;
+
+  const uint32_t bar0 = sb + L::OFF_BAR;
+  const uint32_t q_full = bar0, q_peer = bar0 + 8;
+  auto kv_full = [&](int s) { return bar0 + 8u * (2 + s); };
+  auto kv_peer = [&](int s) { return bar0 + 8u * (2 + L::STAGES + s); };
+  auto kv_empty = [&](int s) { return bar0 + 8u * (2 + 2 * L::STAGES + s); };
+  auto s_full = [&](int k) { return bar0 + 8u * (2 + 3 * L::STAGES + k); };
+  auto s_empty = [&](int k) { return bar0 + 8u * (4 + 3 * L::STAGES + k); };
+  const uint32_t drain = bar0 + 8u * (6 + 3 * L::STAGES);
+  static_assert(2 + 3 * L::STAGES + 4 + 1 == L::NBAR, "barrier region holds every barrier");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
+  volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
+
+  CheckCtx ck{sb, sb + L::OFF_BAR, sb + L::OFF_BAR, sb + L::OFF_BAR + L::NBAR * 8, 0, 0,
+              abort_flag, dev_status};
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    bool lay_ok = true;
+    if (kDeviceChecks) {  // every barrier address inside the barrier region
+      lay_ok = check_bar(ck, q_full, __LINE__) && check_bar(ck, q_peer, __LINE__) &&
+               check_bar(ck, drain, __LINE__);
+      for (int s = 0; s < L::STAGES; ++s)
+        lay_ok = lay_ok && check_bar(ck, kv_full(s), __LINE__) && check_bar(ck, kv_peer(s), __LINE__) &&
+                 check_bar(ck, kv_empty(s), __LINE__);
+      for (int k = 0; k < 2; ++k)
+        lay_ok = lay_ok && check_bar(ck, s_full(k), __LINE__) && check_bar(ck, s_empty(k), __LINE__);
+    }
+    if (lay_ok) {
+      mbar_init(q_full, 1);
+      mbar_init(q_peer, 1);
+      for (int s = 0; s < L::STAGES; ++s) {
+        mbar_init(kv_full(s), 1);
+        mbar_init(kv_peer(s), 1);
+        mbar_init(kv_empty(s), 1);
+      }
+      for (int k = 0; k < 2; ++k) {
+        mbar_init(s_full(k), 1);
+        mbar_init(s_empty(k), 2 * 4 * kGroups);  // one arrival per softmax warp of both CTAs
+      }
+      mbar_init(drain, 1);
+    }
+    *skip_flag = !lay_ok || *reinterpret_cast<volatile int*>(dev_status) != 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tm_q1);
+    tma_prefetch_desc(&tm_k1);
+    tma_prefetch_desc(&tm_q2);
+    tma_prefetch_desc(&tm_k2);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(smem_u32(tmem_slot), 512);
+    tmem_relinquish_pair();
+  }
+  // both CTAs' barriers are initialised before either arrives on the other's
+  tc_fence_before();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (*skip_flag) n_iter = 0;
+  const WaitCtx wc{abort_flag, dev_status, timeout_ns};
+  ck.tmem = tmem;
+  ck.tmem_cols = 512;
+  const int z_hi = static_cast<int>(gridDim.z);
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // this CTA's Q tile once, then its half (keys [64 rank, 64 rank + 64)) of
+    // every key tile through its own ring
+    if (lane == 0 && n_iter > 0) {
+      bool ok = true;
+      if (kDeviceChecks)
+        for (int kb = 0; kb < L::KB; ++kb)
+          ok = ok &&
+               check_tma(ck, sb + L::OFF_Q1 + kb * 16384, 16384, q_full, kb * 64, D, qb * kBlockM,
+                         NQ, kBlockM, bh, z_hi, __LINE__) &&
+               check_tma(ck, sb + L::OFF_Q2 + kb * 16384, 16384, q_full, kb * 64, D, qb * kBlockM,
+                         NQ, kBlockM, bh, z_hi, __LINE__);
+      int it = 0;
+      if (ok) {
+        mbar_arrive_expect_tx(q_full, 2 * L::TILE);
+#pragma unroll
+        for (int kb = 0; kb < L::KB; ++kb) {
+          tma_load_3d(sb + L::OFF_Q1 + kb * 16384, &tm_q1, q_full, kb * 64, qb * kBlockM, bh);
+          tma_load_3d(sb + L::OFF_Q2 + kb * 16384, &tm_q2, q_full, kb * 64, qb * kBlockM, bh);
+        }
+        for (; it < n_iter; ++it) {
+          const int s = it % L::STAGES;
+          if (!wait_bounded(kv_empty(s), ((it / L::STAGES) & 1) ^ 1, wc)) break;
+          const int krow = it * kBlockN + 64 * static_cast<int>(rank);
+          const uint32_t dst = sb + L::OFF_K + s * 2 * L::HALF;
+          bool k_ok = true;
+          if (kDeviceChecks)
+            for (int kb = 0; kb < L::KB; ++kb)
+              k_ok = k_ok &&
+                     check_tma(ck, dst + kb * 8192, 8192, kv_full(s), kb * 64, D, krow, NK, 64, bh,
+                               z_hi, __LINE__) &&
+                     check_tma(ck, dst + L::HALF + kb * 8192, 8192, kv_full(s), kb * 64, D, krow, NK,
+                               64, bh, z_hi, __LINE__);
+          if (!k_ok) break;
+          mbar_arrive_expect_tx(kv_full(s), 2 * L::HALF);
+#pragma unroll
+          for (int kb = 0; kb < L::KB; ++kb) {
+            tma_load_3d(dst + kb * 8192, &tm_k1, kv_full(s), kb * 64, krow, bh);
+            tma_load_3d(dst + L::HALF + kb * 8192, &tm_k2, kv_full(s), kb * 64, krow, bh);
+          }
+        }
+        // let every copy this thread issued land before the CTA can exit
+        wait_drain(q_full, 0, timeout_ns);
+        for (int j = max(0, it - L::STAGES); j < it; ++j)
+          wait_drain(kv_full(j % L::STAGES), (j / L::STAGES) & 1, timeout_ns);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && n_iter > 0 && rank == 0) {
+      // ---------------------------------------------------------- MMA issuer (even CTA)
+      constexpr uint32_t idesc = idesc_bf16(2 * kBlockM, kBlockN, 0, 0);
+      bool ok = check_tmem(ck, tmem, 128, 512, __LINE__) && wait_bounded(q_full, 0, wc) &&
+                wait_bounded(q_peer, 0, wc);
+      tc_fence_after();
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int s = it % L::STAGES;
+        const uint32_t ph = (it / L::STAGES) & 1;
+        const int slot = it & 1;
+        const uint32_t sph = (it >> 1) & 1;
+        if (!(ok = wait_bounded(kv_full(s), ph, wc) && wait_bounded(kv_peer(s), ph, wc))) break;
+        if (!(ok = wait_bounded(s_empty(slot), sph ^ 1, wc))) break;
+        tc_fence_after();
+        const uint32_t kbase = sb + L::OFF_K + s * 2 * L::HALF;
+        const uint32_t d1 = tmem + slot * 256, d2 = d1 + 128;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t qoff = (k >> 2) * 16384 + (k & 3) * 32;
+          const uint32_t koff = (k >> 2) * 8192 + (k & 3) * 32;
+          mma_bf16_pair(d1, smem_desc_sw128(sb + L::OFF_Q1 + qoff, 16, 1024),
+                        smem_desc_sw128(kbase + koff, 16, 1024), idesc, k > 0);
+          mma_bf16_pair(d2, smem_desc_sw128(sb + L::OFF_Q2 + qoff, 16, 1024),
+                        smem_desc_sw128(kbase + L::HALF + koff, 16, 1024), idesc, k > 0);
+        }
+        mma_commit_pair(s_full(slot));
+        mma_commit_pair(kv_empty(s));
+      }
+      mma_commit_pair(drain);
+      wait_drain(drain, 0, timeout_ns);
+    } else if (lane == 0 && n_iter > 0) {
+      // ---------------------------------------------------------- relay (odd CTA)
+      // this CTA's Q tile and key halves have landed: tell the even CTA
+      bool ok = wait_bounded(q_full, 0, wc);
+      if (ok) mbar_arrive_cluster(mapa_shared(q_peer, 0));
+      for (int it = 0; ok && it < n_iter; ++it) {
+        const int s = it % L::STAGES;
+        if (!(ok = wait_bounded(kv_full(s), (it / L::STAGES) & 1, wc))) break;
+        mbar_arrive_cluster(mapa_shared(kv_peer(s), 0));
+      }
+      // the even CTA's MMAs (which read this CTA's shared memory and write
+      // its TMEM) have ended
+      wait_drain(drain, 0, timeout_ns);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ softmax / KL
+    const int grp = (warp - 2) >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qrow = qb * kBlockM + r;
+    const float c = scale * kLog2e;
+    const int lim = causal ? min(NK, qrow + 1 + off) : NK;  // keys < lim visible
+    RowState st{-INFINITY, 0.f, -INFINITY, 0.f, 0.f};
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * 32;
+    for (int it = 0; it < n_iter; ++it) {
+      const int slot = it & 1;
+      const uint32_t sph = (it >> 1) & 1;
+      if (!wait_bounded(s_full(slot), sph, wc)) break;
+      tc_fence_after();
+      float a[32], b[32];
+      const uint32_t ta = lane_base + slot * 256;
+      if (!(check_tmem(ck, ta, 32, 32, __LINE__) && check_tmem(ck, ta + 128, 32, 32, __LINE__)))
+        break;
+      tmem_ld32(ta, a);
+      tmem_ld32(ta + 128, b);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      // S of this slot is in registers (tcgen05.wait::ld above): free it on
+      // the even CTA's barrier; the arrival publishes no memory, so relaxed
+      if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(s_empty(slot), 0));
+      const int key0 = it * kBlockN + grp * 32;
+      if (key0 + 32 <= lim)
+        fold_chunk<false>(a, b, key0, lim, c, st);
+      else
+        fold_chunk<true>(a, b, key0, lim, c, st);
+    }
+    float* xch = reinterpret_cast<float*>(gb + L::OFF_XCH);
+    if (grp > 0) {
+      float* x = xch + (grp - 1) * 5 * kBlockM;
+      x[0 * kBlockM + r] = st.r1;
+      x[1 * kBlockM + r] = st.l1;
+      x[2 * kBlockM + r] = st.r2;
+      x[3 * kBlockM + r] = st.l2;
+      x[4 * kBlockM + r] = st.acc;
+    }
+    named_bar_sync(1, 32 * 4 * kGroups);
+    if (grp == 0) {
+#pragma unroll
+      for (int gq = 0; gq < kGroups - 1; ++gq) {
+        const float* x = xch + gq * 5 * kBlockM;
+        const RowState other{x[0 * kBlockM + r], x[1 * kBlockM + r], x[2 * kBlockM + r],
+                             x[3 * kBlockM + r], x[4 * kBlockM + r]};
+        merge_state(st, other);
+      }
+      if (n_iter > 0 && qrow < NQ) {
+        const size_t o = static_cast<size_t>(bh) * NQ + qrow;
+        float kl, l1, l2;
+        finish_row(st, scale, kl, l1, l2);
+        kl_out[o] = kl;
+        lse1_out[o] = l1;
+        lse2_out[o] = l2;
+      }
+    }
+  }
+
+  // neither CTA releases TMEM or leaves while the pair still works on it
+  tc_fence_before();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+  cluster_sync();
+}
+
 // One thread per (bh, row): merge the split partial states and finish.
 __global__ void streamkl_fwd_combine_kernel(const float* __restrict__ part, int splits,
                                             long long plane, float scale,
@@ -430,6 +719,29 @@ __global__ void streamkl_fwd_combine_kernel(const float* __restrict__ part, int 
   kl_out[i] = kl;
   lse1_out[i] = l1;
   lse2_out[i] = l2;
+}
+
+template <int D>
+cudaError_t launch_fwd_pair_t(const FwdArgs& a, cudaStream_t stream) {
+  using L = PairLayout<D>;
+  auto kern = streamkl_fwd_pair_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::ALLOC);
+  if (e != cudaSuccess) return e;
+  const int nqb = (a.NQ + kBlockM - 1) / kBlockM;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nqb, 1, a.BH);
+  cfg.blockDim = dim3(kFwdThreads, 1, 1);
+  cfg.dynamicSmemBytes = L::ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *a.tm_q1, *a.tm_k1, *a.tm_q2, *a.tm_k2, a.NQ, a.NK, a.causal,
+                            a.scale, a.kl, a.lse1, a.lse2, a.dev_status, a.timeout_ns);
 }
 
 template <int D, bool SPLIT, bool PACKED>
@@ -454,7 +766,13 @@ size_t fwd_smem_bytes(int d) {
   return d == 128 ? FwdLayout<128>::ALLOC : FwdLayout<64>::ALLOC;
 }
 
+bool fwd_pair_eligible(int NQ, int splits, bool packed) {
+  const int nqb = (NQ + kBlockM - 1) / kBlockM;
+  return !packed && splits <= 1 && nqb % 2 == 0;
+}
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+  if (a.pairs) return a.d == 128 ? launch_fwd_pair_t<128>(a, stream) : launch_fwd_pair_t<64>(a, stream);
   const bool split = a.splits > 1;
   if (a.cu_q != nullptr)  // packed batches never split
     return a.d == 128 ? launch_fwd_t<128, false, true>(a, stream) : launch_fwd_t<64, false, true>(a, stream);

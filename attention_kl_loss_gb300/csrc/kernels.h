@@ -85,6 +85,9 @@ struct FwdArgs {
   float* part;  // split partial states, [5][splits][BH][NQ]; null when splits == 1
   int splits;
   int tiles_per_split;
+  // CTA pairs (cta_group::2 MMAs over two query blocks; needs
+  // fwd_pair_eligible): the K maps then have 64-row boxes
+  bool pairs = false;
   int* dev_status;
   uint64_t timeout_ns;
 };
@@ -167,6 +170,7 @@ constexpr int kShortMaxQ = 64;  // query rows the short-sweep kernel handles
 
 // Each returns the launch error (cudaSuccess when queued).
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+bool fwd_pair_eligible(int NQ, int splits, bool packed);
 cudaError_t launch_fwd_combine(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_separate(const BwdSepArgs& a, cudaStream_t stream);

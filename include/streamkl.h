@@ -78,6 +78,27 @@ size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int caus
                                    int num_splits);
 
 /*
+ * Whether the forward runs as CTA pairs for these sizes: 1 = two CTAs of a
+ * thread-block cluster take two query blocks of one (batch, head) slice and
+ * compute their score tiles as one tcgen05 MMA with M = 256 (cta_group::2),
+ * each CTA loading its own query tile and half of every key tile; 0 = one
+ * CTA per query block. Pairs need dense batches without a key split
+ * (num_splits as for streamkl_fwd; 0 = automatic) and an even number of
+ * 128-row query blocks, and are off unless streamkl_set_fwd_pairs(1) was
+ * called (on GB300 they match the one-CTA forward at the 64K causal
+ * workload and are slower on smaller ones). Same results either way up to
+ * fp32 rounding. Returns -1 on invalid sizes. The paper has no counterpart
+ * (it is a scheduling choice of this implementation).
+ */
+int streamkl_fwd_pairs(int B, int H, int NQ, int NK, int d, int causal, int num_splits);
+
+/*
+ * CTA pairs in the forward for the process: 0 = never (default), 1 = when
+ * the sizes allow. Returns 0, or -1 for another value.
+ */
+int streamkl_set_fwd_pairs(int mode);
+
+/*
  * Backward algorithm used for these sizes (gist.science technical summary,
  * section 2, kernel fusion paragraph: a fused kernel with atomic dQ updates,
  * or separate kernels when the atomics contend too much):

@@ -148,6 +148,25 @@ def test_automatic_backward_choice(lib):
         assert lib.streamkl_bwd_algorithm(*args) == 1, args
 
 
+def test_forward_pair_choice(lib):
+    """CTA pairs only when switched on, and then for dense forwards without a
+    split and an even number of 128-row query blocks."""
+    assert lib.streamkl_fwd_pairs(1, 32, 65536, 65536, 128, 1, 0) == 0  # off by default
+    try:
+        assert lib.streamkl_set_fwd_pairs(1) == 0
+        assert lib.streamkl_fwd_pairs(1, 32, 65536, 65536, 128, 1, 0) == 1
+        assert lib.streamkl_fwd_pairs(2, 16, 4096, 4096, 128, 0, 0) == 1
+        assert lib.streamkl_fwd_pairs(1, 2, 200, 300, 64, 1, 0) == 1   # two blocks, ragged
+        assert lib.streamkl_fwd_pairs(1, 2, 300, 300, 64, 1, 0) == 0   # three blocks
+        assert lib.streamkl_fwd_pairs(1, 2, 64, 300, 64, 1, 0) == 0    # one block
+        assert lib.streamkl_fwd_pairs(4, 32, 512, 131072, 128, 1, 0) == 0  # split keys
+        assert lib.streamkl_fwd_pairs(4, 32, 512, 131072, 128, 1, 1) == 1  # forced no split
+        assert lib.streamkl_fwd_pairs(1, 1, 8, 4, 64, 1, 0) == -1
+        assert lib.streamkl_set_fwd_pairs(3) == -1
+    finally:
+        lib.streamkl_set_fwd_pairs(0)
+
+
 def test_dq_key_split_choice(lib):
     """The separate backward's dQ kernel splits its keys only when there are
     few query blocks: never at 64K (16,384 dQ CTAs), at least 2 ways for the

@@ -33,13 +33,15 @@ def test_check_selftest_reports_only_in_the_debug_build():
     assert float(x.sum().item()) == 4.0
 
 
-def _dense_run(w, seed, splits=0, algo=None, dq_splits=None, dk_persist=None, grad2=True):
+def _dense_run(w, seed, splits=0, algo=None, dq_splits=None, dk_persist=None, grad2=True,
+               pairs=None):
     dev = torch.device("cuda")
     q1, k1, q2, k2, g = synthetic.make_inputs(w, seed, dev)
     st = binding.new_status(dev)
     binding.set_bwd_algorithm(algo)
     binding.set_bwd_dq_splits(dq_splits)
     binding.set_bwd_dk_persist(dk_persist)
+    binding.set_fwd_pairs(pairs)
     try:
         kl, l1, l2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, num_splits=splits,
                                           dev_status=st)
@@ -49,6 +51,7 @@ def _dense_run(w, seed, splits=0, algo=None, dq_splits=None, dk_persist=None, gr
         binding.set_bwd_algorithm(None)
         binding.set_bwd_dq_splits(None)
         binding.set_bwd_dk_persist(None)
+        binding.set_fwd_pairs(None)
     binding.raise_on_device_status(st, w.name)
     return (kl, l1, l2) + tuple(grads)
 
@@ -85,6 +88,10 @@ CASES = [
      {"grad2": False}),
     ("short sweep both sets", dict(B=4, H=10, NQ=20, NK=1000, d=128, causal=True, grad1=True), {}),
     ("short sweep one set", dict(B=2, H=3, NQ=64, NK=777, d=128, causal=False), {}),
+    ("forward as CTA pairs", dict(B=2, H=3, NQ=256, NK=333, d=128, causal=True),
+     {"splits": 1, "pairs": True}),
+    ("forward as CTA pairs d64", dict(B=1, H=4, NQ=200, NK=200, d=64, causal=True),
+     {"splits": 1, "pairs": True}),
 ]
 
 

@@ -316,6 +316,37 @@ def test_decode_shape_automatic_paths(algo):
                 assert_grad(host(got[b, hh]), ref, name)
 
 
+@pytest.mark.parametrize("B,H,NQ,NK,d,causal", [(2, 3, 256, 333, 128, True), (1, 4, 200, 200, 64, True),
+                                                 (2, 2, 512, 1000, 128, False), (1, 2, 130, 4096, 128, True)])
+def test_forward_as_cta_pairs(B, H, NQ, NK, d, causal):
+    """The forward as CTA pairs (cta_group::2 MMAs over two query blocks, each
+    CTA holding half of every key tile) against the one-CTA-per-block forward
+    and against the oracle."""
+    w = synthetic.custom(f"pairs_{NQ}x{NK}d{d}", B=B, H=H, NQ=NQ, NK=NK, d=d, causal=causal,
+                         noise=0.4)
+    # no key split (pairs are for unsplit forwards; small shapes would split)
+    assert not binding.fwd_pairs(B, H, NQ, NK, d, causal, num_splits=1)  # off by default
+    dev = torch.device("cuda")
+    q1, k1, q2, k2, _ = synthetic.make_inputs(w, 33, dev)
+    status = binding.new_status(dev)
+    ref = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, num_splits=1, dev_status=status)
+    binding.set_fwd_pairs(True)
+    try:
+        assert binding.fwd_pairs(B, H, NQ, NK, d, causal, num_splits=1)
+        got = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, num_splits=1,
+                                   dev_status=status)
+    finally:
+        binding.set_fwd_pairs(None)
+    binding.raise_on_device_status(status, "forward as CTA pairs")
+    for x, y in zip(got, ref):
+        assert torch.allclose(x, y, rtol=1e-5, atol=1e-6)
+    h = [host(t) for t in (q1, k1, q2, k2)]
+    okl, ol1, ol2 = orc.forward(*h, w.scale, w.causal)
+    assert_kl(got[0].cpu().numpy(), okl)
+    assert rel_l2(got[1].cpu().numpy(), ol1) <= LSE_REL
+    assert rel_l2(got[2].cpu().numpy(), ol2) <= LSE_REL
+
+
 SHORT = [
     # (B, H, N_Q, N_K, causal, sets): decode-like shapes for the fused short-sweep
     # kernel; 40 slices x 8 key tiles = 320 items on 152 CTAs put several
