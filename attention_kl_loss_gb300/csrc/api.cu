@@ -389,8 +389,13 @@ size_t streamkl_fwd_workspace_size(int B, int H, int NQ, int NK, int d, int caus
 size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
   if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return 0;
   const int g1 = want_grad1 ? 1 : 0;
-  if (bwd_algo_impl(B, H, NQ, NK, d, g1) != 0) return bwd_ws(B, H, NQ, NK, d, g1);
-  return dq_split_ws(B, H, NQ, NK, d, 1 + g1);
+  const size_t sep = dq_split_ws(B, H, NQ, NK, d, 1 + g1);
+  if (bwd_algo_impl(B, H, NQ, NK, d, g1) == 0) return sep;
+  const size_t fused = bwd_ws(B, H, NQ, NK, d, g1);
+  // one set under the per-key-tile fused algorithm may be configuration 2
+  // alone, which that kernel hands to the separate kernels
+  if (!g1 && !short_sweep(NQ, d)) return fused > sep ? fused : sep;
+  return fused;
 }
 
 int streamkl_bwd_dq_splits(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
@@ -638,15 +643,17 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   if (!dev_status) return fail(STREAMKL_ERR_INVALID_ARG, "dev_status must be non-NULL");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(STREAMKL_ERR_INVALID_ARG, "scale must be finite and > 0");
   const int grad1 = dq1 != nullptr, grad2 = dq2 != nullptr;
-  // configuration 2 alone always runs the separate kernels (the fused kernel
-  // always produces dQ2/dK2)
-  const int algo = grad2 ? bwd_algo_impl(B, H, NQ, NK, d, grad1) : 0;
+  // configuration 2 alone runs the separate kernels unless the fused
+  // algorithm's short-sweep kernel takes the shape (the per-key-tile fused
+  // kernel always produces dQ2/dK2)
+  int algo = bwd_algo_impl(B, H, NQ, NK, d, grad1);
+  if (!grad2 && !(algo == 1 && short_sweep(NQ, d))) algo = 0;
   // separate kernels: the dQ kernel's key split keeps its fp32 partials in
-  // the workspace; fused kernel: the fp32 dQ accumulators
+  // the workspace; fused kernels: one fp32 dQ accumulator per gradient set
   int dq_splits = 1, dq_per = 0;
   if (algo == 0) dq_split_plan(B, H, NQ, NK, d, grad1 + grad2, &dq_splits, &dq_per);
   const size_t need = algo == 0 ? dq_split_ws(B, H, NQ, NK, d, grad1 + grad2)
-                                : bwd_ws(B, H, NQ, NK, d, grad1);
+                                : bwd_ws(B, H, NQ, NK, d, grad1 && grad2);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
     return fail(STREAMKL_ERR_INVALID_ARG, "backward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
 
@@ -696,7 +703,7 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   }
   cudaError_t e = cudaMemsetAsync(workspace, 0, need, s);
   if (e != cudaSuccess) return cuda_fail(e, "workspace clear");
-  const size_t one = need / (grad1 ? 2 : 1);
+  const size_t one = need / (grad1 + grad2);
   const long long n = static_cast<long long>(BH) * NQ * d;
   if (short_kernel) {
     skl::BwdShortArgs a{};
@@ -717,15 +724,19 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
     a.g = dkl;
     a.dk2 = dk2;
     a.dk1 = dk1;
-    a.dq2acc = static_cast<float*>(workspace);
-    a.dq1acc = grad1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + one) : nullptr;
+    // the accumulators of the sets computed, set 2's first
+    a.dq2acc = grad2 ? static_cast<float*>(workspace) : nullptr;
+    a.dq1acc = grad1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + (grad2 ? one : 0))
+                     : nullptr;
     a.ctas = num_sms();
     a.dev_status = dev_status;
     a.timeout_ns = wait_timeout_ns();
     e = skl::launch_bwd_short(a, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-    e = skl::launch_dq_convert(a.dq2acc, dq2, n, s);
-    if (e != cudaSuccess) return cuda_fail(e, "dq2 convert launch");
+    if (grad2) {
+      e = skl::launch_dq_convert(a.dq2acc, dq2, n, s);
+      if (e != cudaSuccess) return cuda_fail(e, "dq2 convert launch");
+    }
     if (grad1) {
       e = skl::launch_dq_convert(a.dq1acc, dq1, n, s);
       if (e != cudaSuccess) return cuda_fail(e, "dq1 convert launch");

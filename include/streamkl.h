@@ -163,7 +163,8 @@ int streamkl_set_bwd_dk_persist(int ctas);
  * want_grad1 != 0, both (an upper bound for configuration 2 alone): for the
  * separate-kernel algorithm the fp32 partials of the dQ kernel's key split
  * (0 without a split); for the fused one, one fp32 [B, H, N_Q, d] dQ
- * accumulator per requested gradient set.
+ * accumulator per requested gradient set (with want_grad1 = 0 also enough
+ * for configuration 2 alone where that runs the separate kernels).
  */
 size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int causal,
                                    int want_grad1);
@@ -235,8 +236,9 @@ streamkl_status streamkl_fwd_noalloc(const void* q1, const void* k1, const void*
  *   out: dq2 [B,H,N_Q,d], dk2 [B,H,N_K,d] (bf16) for configuration 1;
  *        dq1, dk1 likewise for configuration 2. Either pair may be NULL to
  *        skip that configuration (both of a pair NULL or neither; at least one
- *        pair is required). Configuration 2 alone always runs the separate
- *        dK/dQ kernels.
+ *        pair is required). Configuration 2 alone runs the separate dK/dQ
+ *        kernels, or the fused algorithm's short-sweep kernel where that is
+ *        the algorithm chosen (at most 64 query rows at d = 128).
  *   workspace: ws_bytes >= streamkl_bwd_workspace_size(..., want_grad1) (may be
  *        NULL when that is 0); the call clears the part it uses (stream-ordered).
  */

@@ -118,9 +118,17 @@ def test_workspace_sizes(lib):
         assert lib.streamkl_set_bwd_algorithm(1) == 0  # fused: fp32 dQ accumulators
         assert lib.streamkl_bwd_algorithm(1, 32, 65536, 65536, 128, 1, 1) == 1
         assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 1) == 2 * 32 * 65536 * 128 * 4
-        assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 0) == 32 * 65536 * 128 * 4
+        # one set under the per-key-tile fused kernel may be configuration 2
+        # alone, which runs the separate kernels: room for their dQ partials too
+        dq1 = lib.streamkl_bwd_dq_splits(1, 32, 65536, 65536, 128, 1, 0)
+        assert lib.streamkl_bwd_workspace_size(1, 32, 65536, 65536, 128, 1, 0) == max(
+            32 * 65536 * 128 * 4, dq1 * 32 * 65536 * 128 * 4 if dq1 > 1 else 0)
+        dq = lib.streamkl_bwd_dq_splits(4, 32, 512, 131072, 128, 1, 0)
+        dq_ws = dq * 128 * 512 * 128 * 4 if dq > 1 else 0
         assert lib.streamkl_workspace_size(4, 32, 512, 131072, 128, 1, 0) == max(
-            5 * s * 128 * 512 * 4, 128 * 512 * 128 * 4)
+            5 * s * 128 * 512 * 4, 128 * 512 * 128 * 4, dq_ws)
+        # the short-sweep kernel takes either set alone: one accumulator
+        assert lib.streamkl_bwd_workspace_size(2, 8, 64, 65536, 128, 1, 0) == 2 * 8 * 64 * 128 * 4
         # separate: only the dQ kernel's key-split partials
         assert lib.streamkl_set_bwd_algorithm(0) == 0
         assert lib.streamkl_bwd_algorithm(1, 32, 65536, 65536, 128, 1, 1) == 0

@@ -88,6 +88,8 @@ CASES = [
      {"grad2": False}),
     ("short sweep both sets", dict(B=4, H=10, NQ=20, NK=1000, d=128, causal=True, grad1=True), {}),
     ("short sweep one set", dict(B=2, H=3, NQ=64, NK=777, d=128, causal=False), {}),
+    ("short sweep configuration 2 only", dict(B=2, H=3, NQ=48, NK=2000, d=128, causal=True,
+                                               grad1=True), {"grad2": False}),
     ("forward as CTA pairs", dict(B=2, H=3, NQ=256, NK=333, d=128, causal=True),
      {"splits": 1, "pairs": True}),
     ("forward as CTA pairs d64", dict(B=1, H=4, NQ=200, NK=200, d=64, causal=True),
@@ -103,7 +105,7 @@ def test_debug_build_passes_its_checks_and_matches_release(name, shape, opts):
         got = _dense_run(w, 31, **opts)
     fused = opts.get("algo", binding.bwd_algorithm(w.B, w.H, w.NQ, w.NK, w.d, w.causal,
                                                   w.grad1)) == binding.BWD_FUSED
-    _same(got, ref, name, atomic_dq=fused and opts.get("grad2", True))
+    _same(got, ref, name, atomic_dq=fused)
 
 
 @pytest.mark.parametrize("causal", [False, True])

@@ -357,6 +357,7 @@ SHORT = [
     (2, 2, 33, 200, True, "config1"),
     (4, 10, 20, 1000, True, "both"),
     (4, 10, 64, 1000, False, "config1"),
+    (2, 3, 48, 2000, True, "config2"),
 ]
 
 
@@ -366,21 +367,26 @@ def test_short_sweep_fused_backward(B, H, NQ, NK, causal, sets):
     128: one visit per (query, key) pair, dQ kept on chip per batch-head)
     against the oracle, slice by slice, and the library choosing it."""
     w = synthetic.custom(f"short_{B}x{H}x{NQ}x{NK}", B=B, H=H, NQ=NQ, NK=NK, d=128, causal=causal,
-                         noise=0.4, grad1=sets == "both")
+                         noise=0.4, grad1=sets != "config1")
+    grad2 = sets != "config2"
     assert binding.bwd_algorithm(B, H, NQ, NK, 128, causal, w.grad1) == binding.BWD_FUSED
     dev = torch.device("cuda")
     q1, k1, q2, k2, _ = synthetic.make_inputs(w, 29, dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(30)
     g = torch.randn((B, H, NQ), generator=gen, device=dev, dtype=torch.float32)
-    ins, outs, grads = run(w, inputs=(q1, k1, q2, k2, g))
+    status = binding.new_status(dev)
+    kl, lse1, lse2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, dev_status=status)
+    grads = binding.streamkl_bwd(q1, k1, q2, k2, kl, lse1, lse2, g, w.scale, w.causal,
+                                 grad1=w.grad1, grad2=grad2, dev_status=status)
+    binding.raise_on_device_status(status, "short sweep")
     for b in range(B):
         for hh in range(H):
-            h = [host(t[b, hh]) for t in ins[:4]]
+            h = [host(t[b, hh]) for t in (q1, k1, q2, k2)]
             og = orc.head_backward(*h, w.scale, w.causal, g[b, hh].cpu().numpy().astype(np.float64),
                                    w.grad1)
             for i, name in enumerate(["dq2", "dk2", "dq1", "dk1"]):
-                if og[i] is None:
+                if og[i] is None or (i < 2 and not grad2):
                     assert grads[i] is None
                     continue
                 assert_grad(host(grads[i][b, hh]), og[i], f"{name} slice {b},{hh}")
