@@ -20,7 +20,9 @@
  *   j <= i + (N_K - N_Q) (j <= i when N_Q == N_K); it needs N_Q <= N_K.
  * - All pointers are device pointers owned by the caller. The library
  *   allocates no memory, never synchronises, and enqueues all work on
- *   `stream` (a cudaStream_t; NULL means the legacy default stream).
+ *   `stream` (a cudaStream_t; NULL means the legacy default stream), so the
+ *   calls can be captured into a CUDA graph once their kernels have run
+ *   eagerly (the first call sets their shared-memory attributes).
  * - Synchronous argument errors return STREAMKL_ERR_INVALID_ARG or
  *   STREAMKL_ERR_UNSUPPORTED before anything is enqueued; a failed launch
  *   returns STREAMKL_ERR_CUDA. streamkl_last_error() gives the detail.

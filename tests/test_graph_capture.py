@@ -58,3 +58,69 @@ def test_captured_step_replays_like_eager(NQ, NK, d, causal, grad1):
         binding.raise_on_device_status(status, "graph replay")
         for a, b in zip(got, ref):
             assert torch.equal(a, b)
+
+
+# (name, shape): separate kernels, split forward with a workspace, and the
+# short-sweep fused backward (its dQ summed with fp32 reductions)
+CASES = [
+    ("separate", dict(B=2, H=3, NQ=300, NK=333, d=128, causal=True, grad1=True)),
+    ("split forward d64", dict(B=1, H=4, NQ=64, NK=8192, d=64, causal=True)),
+    ("short sweep", dict(B=2, H=8, NQ=48, NK=4000, d=128, causal=True, grad1=True)),
+]
+
+
+def _step(w, ins, status):
+    q1, k1, q2, k2, g = ins
+    out = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, dev_status=status)
+    grads = binding.streamkl_bwd(q1, k1, q2, k2, *out, g, w.scale, w.causal, grad1=w.grad1,
+                                 dev_status=status)
+    return tuple(out) + tuple(grads)
+
+
+def _close(got, want, what, atomic_dq):
+    for i, (x, y) in enumerate(zip(got, want)):
+        assert (x is None) == (y is None), (what, i)
+        if x is None:
+            continue
+        if atomic_dq and i in (3, 5):
+            err = (x.double() - y.double()).norm() / max(float(y.double().norm()), 1e-30)
+            assert float(err) <= 1e-3, (what, i, float(err))
+        else:
+            assert torch.equal(x, y), (what, i)
+
+
+@pytest.mark.parametrize("name,shape", CASES, ids=[c[0] for c in CASES])
+def test_captured_step_with_binding_allocations(name, shape):
+    """Outputs and workspace allocated by the binding inside the capture (from
+    the graph's memory pool), on the separate, split-forward and short-sweep
+    paths; the short-sweep dQ is summed with fp32 reductions, so it matches
+    to rounding."""
+    w = synthetic.custom(name.replace(" ", "_"), noise=0.3, **shape)
+    dev = torch.device("cuda")
+    ins = synthetic.make_inputs(w, 41, dev)
+    status = binding.new_status(dev)
+    fused = binding.bwd_algorithm(w.B, w.H, w.NQ, w.NK, w.d, w.causal, w.grad1) == binding.BWD_FUSED
+    if name == "split forward d64":
+        assert binding.choose_splits(w.B, w.H, w.NQ, w.NK, w.d, w.causal) > 1
+
+    eager = _step(w, ins, status)  # also loads every kernel before the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        captured = _step(w, ins, status)
+    graph.replay()
+    torch.cuda.synchronize()
+    binding.raise_on_device_status(status, name)
+    _close(captured, eager, f"{name}: replay", fused)
+
+    # new values in the same buffers: the replay reads them
+    fresh = synthetic.make_inputs(w, 42, dev)
+    for dst, src in zip(ins, fresh):
+        dst.copy_(src)
+    graph.replay()
+    torch.cuda.synchronize()
+    again = _step(w, ins, status)
+    torch.cuda.synchronize()
+    binding.raise_on_device_status(status, name)
+    _close(captured, again, f"{name}: replay on new inputs", fused)
+    assert not torch.equal(captured[0], eager[0])

@@ -21,7 +21,7 @@ def _rel_l2(got, ref):
     return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
 
 
-def _run(lens_q, lens_k, H, d, causal, seed=5, grad1=True):
+def _run(lens_q, lens_k, H, d, causal, seed=5, grad1=True, grad2=True):
     dev = torch.device("cuda")
     q1, k1, q2, k2, g, cu_q, cu_k = synthetic.make_packed_inputs(lens_q, lens_k, H, d, seed,
                                                                  device=dev)
@@ -31,7 +31,7 @@ def _run(lens_q, lens_k, H, d, causal, seed=5, grad1=True):
     kl, l1, l2 = binding.streamkl_fwd_varlen(q1, k1, q2, k2, cu_q, cu_k, mq, mk, scale, causal,
                                              dev_status=st)
     grads = binding.streamkl_bwd_varlen(q1, k1, q2, k2, cu_q, cu_k, mq, mk, kl, l1, l2, g, scale,
-                                        causal, grad1=grad1, dev_status=st)
+                                        causal, grad1=grad1, grad2=grad2, dev_status=st)
     torch.cuda.synchronize()
     return (q1, k1, q2, k2, g, cu_q.tolist(), cu_k.tolist(), scale), (kl, l1, l2), grads, st
 
@@ -67,6 +67,39 @@ def test_packed_batch_matches_oracle_per_sequence(d, causal):
                     assert np.max(np.abs(got)) <= 1e-5, (b, h, name)
                 else:
                     assert _rel_l2(got, ref) <= GRAD_REL, (b, h, name, _rel_l2(got, ref))
+
+
+@pytest.mark.parametrize("d,causal", [(128, True), (64, False)])
+@pytest.mark.parametrize("sets", ["config1", "config2"])
+def test_packed_batch_one_gradient_set(sets, d, causal):
+    """Either configuration alone on a packed batch: the requested pair
+    against the oracle, the other pair not produced."""
+    lens_q, lens_k = [70, 0, 257, 3], [90, 5, 300, 64]
+    grad1, grad2 = sets == "config2", sets == "config1"
+    ins, (kl, l1, l2), grads, st = _run(lens_q, lens_k, 2, d, causal, seed=8, grad1=grad1,
+                                        grad2=grad2)
+    assert int(st.item()) == 0
+    assert (grads[0] is None) == (not grad2) and (grads[2] is None) == (not grad1)
+    q1, k1, q2, k2, g, cu_q, cu_k, scale = ins
+    for b in range(len(lens_q)):
+        qs, qe, ks, ke = cu_q[b], cu_q[b + 1], cu_k[b], cu_k[b + 1]
+        for h in range(2):
+            if qe == qs:
+                for t in (grads[1], grads[3]):
+                    if t is not None:
+                        assert torch.all(t[ks:ke, h].float() == 0), b
+                continue
+            sl = [_f64(t[a:e, h]) for t, a, e in ((q1, qs, qe), (k1, ks, ke), (q2, qs, qe),
+                                                  (k2, ks, ke))]
+            og = orc.head_backward(*sl, scale, causal, _f64(g[qs:qe, h]), True)
+            for i, (lo, hi) in enumerate(((qs, qe), (ks, ke), (qs, qe), (ks, ke))):
+                if grads[i] is None:
+                    continue
+                got, ref = _f64(grads[i][lo:hi, h]), og[i]
+                if not np.any(ref):
+                    assert np.max(np.abs(got)) <= 1e-5, (b, h, i)
+                else:
+                    assert _rel_l2(got, ref) <= GRAD_REL, (b, h, i, _rel_l2(got, ref))
 
 
 def test_single_sequence_equals_dense_api():
