@@ -724,6 +724,12 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
     a.g = dkl;
     a.dk2 = dk2;
     a.dk1 = dk1;
+    // dK leaves through TMA stores of 128-row tiles
+    CUtensorMap mdk2, mdk1;
+    if (grad2 && (st = make_map(&mdk2, dk2, BH, NK, d, "dk2", skl::kBlockN)) != STREAMKL_OK) return st;
+    if (grad1 && (st = make_map(&mdk1, dk1, BH, NK, d, "dk1", skl::kBlockN)) != STREAMKL_OK) return st;
+    a.tm_dk2 = grad2 ? &mdk2 : &mdk1;
+    a.tm_dk1 = grad1 ? &mdk1 : &mdk2;
     // the accumulators of the sets computed, set 2's first
     a.dq2acc = grad2 ? static_cast<float*>(workspace) : nullptr;
     a.dq1acc = grad1 ? reinterpret_cast<float*>(static_cast<char*>(workspace) + (grad2 ? one : 0))

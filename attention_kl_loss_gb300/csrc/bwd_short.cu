@@ -31,7 +31,11 @@
 // epilogues: warp w reads TMEM lanes [32 (w%4), +32) and serves column group
 // g = (w-2)/4; thread = key row (TMEM lane) of T, owning query columns
 // [16g, 16g+16), and d columns [32g, 32g+32) of its dK row; for the dQ^T
-// read-out, thread = one d column (lane), queries [16g, 16g+16).
+// read-out, thread = one d column (lane), queries [16g, 16g+16); 18 = dK
+// stores (lane 0). dK leaves through a 32 KB staging tile in shared memory
+// (128-byte swizzle, the softmax warps write their rows' pieces) and two TMA
+// stores per tile, so the writes are whole lines instead of one 16-byte piece
+// of a different row per thread.
 // TMEM: T1 [0,64) T2 [64,128) | dK set 2 [128,256) set 1 [256,384) |
 // dQ^T set 2 [384,448) set 1 [448,512).
 #include "kernels.h"
@@ -41,8 +45,9 @@ namespace skl {
 
 namespace {
 
-constexpr int kShThreads = 576;  // 18 warps
+constexpr int kShThreads = 608;  // 19 warps
 constexpr int kShSoftmaxWarps = 16;
+constexpr int kShStoreWarp = 18;
 constexpr int kShQ = 64;          // query rows per item (padded with zero rows)
 constexpr int kShD = 128;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -58,18 +63,21 @@ struct ShortLayout {
   static constexpr int OFF_Q = 0;                  // Q1, Q2
   static constexpr int OFF_K = 2 * QT;             // stage s: K1 at +2s KT, K2 at +(2s+1) KT
   static constexpr int OFF_DS = OFF_K + STAGES * 2 * KT;  // slot t: the t-th computed set
-  static constexpr int OFF_TAB = OFF_DS + NSETS * DST;    // [4][64] float
+  static constexpr int STG = kBlockN * kShD * 2;          // dK staging: 2 boxes of 128 rows x 128 B
+  static constexpr int OFF_STG = OFF_DS + NSETS * DST;
+  static constexpr int OFF_TAB = OFF_STG + STG;           // [4][64] float
   static constexpr int OFF_BAR = OFF_TAB + 4 * kShQ * 4;
   // q_full, q_empty, tab_free, k_full[2], k_empty[2], t_full, t_free, ds_full,
-  // ds_free, dk_full, dk_free, dq_full, dq_free, drain
-  static constexpr int NBAR = 3 + 2 * STAGES + 9;
+  // ds_free, dk_full, dk_free, dq_full, dq_free, drain, st_full, st_empty
+  static constexpr int NBAR = 3 + 2 * STAGES + 11;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;
   static constexpr uint32_t COL_T = 0, COL_DK = 128, COL_DQ = 384;
   static_assert(COL_DQ + NSETS * kShQ <= 512, "TMEM budget");
   static_assert(ALLOC <= 232448, "shared memory budget");
-  static_assert(OFF_DS % 1024 == 0 && OFF_K % 1024 == 0, "swizzled tiles on 1024-byte boundaries");
+  static_assert(OFF_DS % 1024 == 0 && OFF_K % 1024 == 0 && OFF_STG % 1024 == 0,
+                "swizzled tiles on 1024-byte boundaries");
 };
 
 template <int SETS>
@@ -81,7 +89,8 @@ __global__ void __launch_bounds__(kShThreads, 1)
                               int causal, float scale, int BH, int items_per_cta,
                               const float* __restrict__ kl_in, const float* __restrict__ lse1_in,
                               const float* __restrict__ lse2_in, const float* __restrict__ g_in,
-                              __nv_bfloat16* __restrict__ dk2, __nv_bfloat16* __restrict__ dk1,
+                              const __grid_constant__ CUtensorMap tm_dk2,
+                              const __grid_constant__ CUtensorMap tm_dk1,
                               float* __restrict__ dq2acc, float* __restrict__ dq1acc,
                               int* dev_status, uint64_t timeout_ns) {
   using L = ShortLayout<SETS>;
@@ -114,7 +123,9 @@ __global__ void __launch_bounds__(kShThreads, 1)
   const uint32_t t_free = t_full + 8, ds_full = t_full + 16, ds_free = t_full + 24;
   const uint32_t dk_full = t_full + 32, dk_free = t_full + 40;
   const uint32_t dq_full = t_full + 48, dq_free = t_full + 56, drain = t_full + 64;
-  static_assert(3 + 2 * L::STAGES + 9 == L::NBAR, "barrier region holds every barrier");
+  // staging tile written by the softmax warps / read by the store warp's TMA stores
+  const uint32_t st_full = t_full + 72, st_empty = t_full + 80;
+  static_assert(3 + 2 * L::STAGES + 11 == L::NBAR, "barrier region holds every barrier");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
   volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
@@ -129,7 +140,8 @@ __global__ void __launch_bounds__(kShThreads, 1)
     if (kDeviceChecks) {  // every barrier address inside the barrier region
       lay_ok = check_bar(ck, q_full, __LINE__) && check_bar(ck, q_empty, __LINE__) &&
                check_bar(ck, tab_free, __LINE__) && check_bar(ck, t_full, __LINE__) &&
-               check_bar(ck, drain, __LINE__);
+               check_bar(ck, drain, __LINE__) && check_bar(ck, st_full, __LINE__) &&
+               check_bar(ck, st_empty, __LINE__);
       for (int s = 0; s < L::STAGES; ++s)
         lay_ok = lay_ok && check_bar(ck, k_full(s), __LINE__) && check_bar(ck, k_empty(s), __LINE__);
     }
@@ -150,6 +162,8 @@ __global__ void __launch_bounds__(kShThreads, 1)
       mbar_init(dq_full, 1);
       mbar_init(dq_free, kShSoftmaxWarps);
       mbar_init(drain, 1);
+      mbar_init(st_full, kShSoftmaxWarps);
+      mbar_init(st_empty, 1);
     }
     // a failure recorded earlier (this launch or a previous one), or a
     // failed layout check, skips the work
@@ -161,6 +175,10 @@ __global__ void __launch_bounds__(kShThreads, 1)
     tma_prefetch_desc(&tm_k1);
     tma_prefetch_desc(&tm_q2);
     tma_prefetch_desc(&tm_k2);
+  }
+  if (warp == kShStoreWarp && lane == 0) {
+    if (HAS2) tma_prefetch_desc(&tm_dk2);
+    if (HAS1) tma_prefetch_desc(&tm_dk1);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -288,19 +306,26 @@ __global__ void __launch_bounds__(kShThreads, 1)
           tc_fence_after();
           issue_t(it);
         }
-        // T of the next item of the same batch-head as soon as the softmax
-        // warps have loaded this one (its K tile is the other stage)
+        // gradient GEMMs of this item as soon as its dS is in shared memory
+        // (slot t holds the t-th computed set: set 2 first when present).
+        // While the softmax warps still compute that dS, T of the next item of
+        // the same batch-head goes in if it can (its K tile has landed in the
+        // other stage and the softmax warps have loaded this T); otherwise it
+        // waits for the next round, so a late K tile never holds up this
+        // item's dK, which the softmax warps read next.
         t_issued_next = false;
-        if (it + 1 < n && !seg_start(it + 1)) {
-          if (!(ok = wait_bounded(k_full((it + 1) % L::STAGES), ((it + 1) / L::STAGES) & 1, wc))) break;
-          if (!(ok = wait_bounded(t_free, it & 1, wc))) break;
-          tc_fence_after();
-          issue_t(it + 1);
-          t_issued_next = true;
-        }
-        // gradient GEMMs of this item once its dS is in shared memory (slot t
-        // holds the t-th computed set: set 2 first when present)
-        if (!(ok = wait_bounded(ds_full, it & 1, wc))) break;
+        const bool can_next = it + 1 < n && !seg_start(it + 1);
+        const int sn = (it + 1) % L::STAGES;
+        const uint32_t phn = ((it + 1) / L::STAGES) & 1;
+        auto try_next = [&]() {
+          if (can_next && !t_issued_next && mbar_test_wait(k_full(sn), phn) &&
+              mbar_test_wait(t_free, it & 1)) {
+            tc_fence_after();
+            issue_t(it + 1);
+            t_issued_next = true;
+          }
+        };
+        if (!(ok = wait_bounded_idle(ds_full, it & 1, wc, try_next))) break;
         if (it > 0 && !(ok = wait_bounded(dk_free, (it - 1) & 1, wc))) break;
         tc_fence_after();
         const uint32_t ks = sb + L::OFF_K + s * 2 * L::KT;
@@ -337,6 +362,27 @@ __global__ void __launch_bounds__(kShThreads, 1)
       }
       mma_commit(drain);
       wait_drain(drain, 0, timeout_ns);
+    }
+  } else if (warp == kShStoreWarp) {
+    // ------------------------------------------------------------ dK stores
+    if (lane == 0 && n > 0) {
+      bool ok = true;
+      int u = 0;  // staging uses so far
+      for (int it = 0; ok && it < n; ++it) {
+        const int bh = item_bh(it), kt = item_kt(it);
+        for (int t = 0; t < L::NSETS; ++t, ++u) {
+          if (!(ok = wait_bounded(st_full, u & 1, wc))) break;
+          // rows past N_K (the last tile's tail) are not written by the store
+          if (!(ok = dcheck(ck, kt * kBlockN < NK && bh < BH, __LINE__))) break;
+          const CUtensorMap* m = (HAS2 && t == 0) ? &tm_dk2 : &tm_dk1;
+          tma_store_3d(m, sb + L::OFF_STG, 0, kt * kBlockN, bh);
+          tma_store_3d(m, sb + L::OFF_STG + L::STG / 2, 64, kt * kBlockN, bh);
+          bulk_commit_group();
+          bulk_wait_read_all();  // the tile may be written again
+          mbar_arrive(st_empty);
+        }
+      }
+      bulk_wait_all();  // every dK tile is in global memory before the CTA exits
     }
   } else {
     // ------------------------------------------------------------ softmax / epilogues
@@ -429,25 +475,31 @@ __global__ void __launch_bounds__(kShThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full);
-      // dK of this key row: d columns [32 grp, 32 grp + 32) of each set
+      // dK of this key row: d columns [32 grp, 32 grp + 32) of each set, to
+      // the staging tile (box grp/2, 16-byte chunks 4 (grp%2) .. +4 of the
+      // row, swizzled by the row); the store warp writes the tile out
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(dk_full, it & 1, wc)))) break;
       tc_fence_after();
+      const uint32_t srow = sb + L::OFF_STG + (grp >> 1) * (L::STG / 2) + static_cast<uint32_t>(r * 128);
 #pragma unroll
       for (int t = 0; t < L::NSETS; ++t) {
-        __nv_bfloat16* out = (HAS2 && t == 0) ? dk2 : dk1;
         float v[32];
-        if (!check_tmem(ck, tmem + lane_off + L::COL_DK + t * D + grp * 32, 32, 32, __LINE__)) break;
+        if (!(ok = check_tmem(ck, tmem + lane_off + L::COL_DK + t * D + grp * 32, 32, 32, __LINE__))) break;
         tmem_ld32(tmem + lane_off + L::COL_DK + t * D + grp * 32, v);
         tmem_wait_ld();
-        if (key < NK) {
-          uint4* dst = reinterpret_cast<uint4*>(out + (static_cast<size_t>(bh) * NK + key) * D + grp * 32);
+        // the store warp has read the tile's previous contents
+        const int u = it * L::NSETS + t;
+        if (!(ok = __all_sync(0xffffffffu, wait_bounded(st_empty, (u & 1) ^ 1, wc)))) break;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            dst[j] = make_uint4(pack_bf16x2(v[8 * j], v[8 * j + 1]), pack_bf16x2(v[8 * j + 2], v[8 * j + 3]),
-                                pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
-                                pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
-        }
+        for (int j = 0; j < 4; ++j)
+          st_shared_v4(srow + ((((grp & 1) * 4 + j) ^ (r & 7)) << 4), pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                       pack_bf16x2(v[8 * j + 2], v[8 * j + 3]), pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                       pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(st_full);
       }
+      if (!ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dk_free);
@@ -495,8 +547,7 @@ cudaError_t launch_short_t(const BwdShortArgs& a, cudaStream_t stream) {
   const int grid = static_cast<int>((n_items + per - 1) / per);
   kern<<<grid, kShThreads, L::ALLOC, stream>>>(
       *a.tm_q1, *a.tm_k1, *a.tm_q2, *a.tm_k2, a.NQ, a.NK, a.causal, a.scale, a.BH, per, a.kl,
-      a.lse1, a.lse2, a.g, static_cast<__nv_bfloat16*>(a.dk2), static_cast<__nv_bfloat16*>(a.dk1),
-      a.dq2acc, a.dq1acc, a.dev_status, a.timeout_ns);
+      a.lse1, a.lse2, a.g, *a.tm_dk2, *a.tm_dk1, a.dq2acc, a.dq1acc, a.dev_status, a.timeout_ns);
   return cudaGetLastError();
 }
 

@@ -160,6 +160,8 @@ struct BwdShortArgs {
   const float* g;
   void* dk2;       // bf16 [BH][NK][d]
   void* dk1;
+  const CUtensorMap* tm_dk2;  // the dK outputs, 64-column x 128-row boxes (a
+  const CUtensorMap* tm_dk1;  // set not computed: any valid map, never used)
   float* dq2acc;   // fp32 [BH][NQ][d]
   float* dq1acc;
   int ctas;        // persistent grid size (one CTA per SM)

@@ -103,6 +103,24 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   }
 }
 
+// wait_bounded() that runs idle() between polls: work that may go ahead while
+// the phase is pending (idle() itself must never block).
+template <typename F>
+__device__ __forceinline__ bool wait_bounded_idle(uint32_t bar, uint32_t parity, const WaitCtx& w,
+                                                  F&& idle) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    idle();
+    if (mbar_test_wait(bar, parity)) return true;
+    if (*w.abort_flag) return false;
+    if (global_timer_ns() - t0 > w.timeout_ns) {
+      *w.abort_flag = 1;
+      atomicCAS(w.dev_status, 0, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- debug checks
 // The debug build checks the operands of every TMA copy, TMEM access and
 // mbarrier operation against the kernel's layout before it is issued. A
@@ -197,6 +215,28 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
+}
+
+// 3-D tiled store shared -> global in this thread's bulk async-group. c0 as
+// for tma_load_3d; c1, c2 must not be negative (rows past the tensor's end
+// are not written).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(src), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// This thread's committed bulk stores are complete (written to global memory).
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async
