@@ -308,6 +308,25 @@ streamkl_status make_map(CUtensorMap* m, const void* ptr, int BH, int N, int d, 
   return STREAMKL_OK;
 }
 
+// 4-D map {d, N, BH, planes} of fp32 [planes][BH][N][d] rows (the dQ split's
+// partials): 32-column (128-byte) x 128-row boxes, 128-byte swizzle, so a
+// store of a 128-row tile stops at the end of its own (plane, batch-head).
+streamkl_status make_map_part(CUtensorMap* m, void* ptr, int planes, int BH, int N, int d) {
+  auto enc = encode_fn();
+  if (!enc) return fail(STREAMKL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  const cuuint64_t gdim[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH), static_cast<cuuint64_t>(planes)};
+  const cuuint64_t gstride[3] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4,
+                                 static_cast<cuuint64_t>(BH) * N * d * 4};
+  const cuuint32_t box[4] = {32, static_cast<cuuint32_t>(skl::kBlockM), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, gdim, gstride, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(STREAMKL_ERR_CUDA, "tensor map for the dQ partials failed (CUresult %d)", static_cast<int>(r));
+  return STREAMKL_OK;
+}
+
 // 3-D map {d, total, H} of a packed [total, H, d] bf16 tensor: rows of one
 // head are H d elements apart. 64-column x box_rows boxes, 128-byte swizzle.
 streamkl_status make_map_packed(CUtensorMap* m, const void* ptr, int total, int H, int d,
@@ -695,6 +714,25 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
     a.dk2 = dk2;
     a.dq1 = dq1;
     a.dk1 = dk1;
+    // the outputs leave the kernels through TMA stores of 128-row tiles
+    CUtensorMap mdk2, mdk1, mdq2, mdq1, mpart;
+    if (grad2) {
+      if ((st = make_map(&mdk2, dk2, BH, NK, d, "dk2", skl::kBlockM)) != STREAMKL_OK) return st;
+      if ((st = make_map(&mdq2, dq2, BH, NQ, d, "dq2", skl::kBlockM)) != STREAMKL_OK) return st;
+    }
+    if (grad1) {
+      if ((st = make_map(&mdk1, dk1, BH, NK, d, "dk1", skl::kBlockM)) != STREAMKL_OK) return st;
+      if ((st = make_map(&mdq1, dq1, BH, NQ, d, "dq1", skl::kBlockM)) != STREAMKL_OK) return st;
+    }
+    a.tm_dk2 = grad2 ? &mdk2 : &mdk1;
+    a.tm_dk1 = grad1 ? &mdk1 : &mdk2;
+    a.tm_dq2 = grad2 ? &mdq2 : &mdq1;
+    a.tm_dq1 = grad1 ? &mdq1 : &mdq2;
+    if (dq_splits > 1) {
+      if ((st = make_map_part(&mpart, workspace, (grad1 + grad2) * dq_splits, BH, NQ, d)) != STREAMKL_OK)
+        return st;
+      a.tm_part = &mpart;
+    }
     a.dev_status = dev_status;
     a.timeout_ns = wait_timeout_ns();
     cudaError_t e = skl::launch_bwd_separate(a, s);

@@ -91,8 +91,9 @@ struct SepLayout {
   static constexpr int TAB_BYTES = DQ ? 0 : STAGES * 4 * STEP * 4;
   static constexpr int OFF_BAR = OFF_TAB + TAB_BYTES;
   // x_full, y_full[S], y_empty[S], s_full, s_free, ds_full[2], ds_free[2],
-  // acc_full, drain, x_free, acc_empty (the last two: persistent kernel)
-  static constexpr int NBAR = 1 + 2 * STAGES + 10;
+  // acc_full, drain, x_free, acc_empty (these two: persistent kernel), ep_full,
+  // ep_empty (output staging)
+  static constexpr int NBAR = 1 + 2 * STAGES + 12;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;
@@ -128,7 +129,9 @@ __global__ void __launch_bounds__(kSepThreads, 1)
     streamkl_bwd_sep_kernel(const __grid_constant__ CUtensorMap tm_x1,
                             const __grid_constant__ CUtensorMap tm_x2,
                             const __grid_constant__ CUtensorMap tm_y1,
-                            const __grid_constant__ CUtensorMap tm_y2, int NQ, int NK,
+                            const __grid_constant__ CUtensorMap tm_y2,
+                            const __grid_constant__ CUtensorMap tm_o2,
+                            const __grid_constant__ CUtensorMap tm_o1, int NQ, int NK,
                             int causal, float scale, const float* __restrict__ kl_in,
                             const float* __restrict__ lse1_in, const float* __restrict__ lse2_in,
                             const float* __restrict__ g_in, __nv_bfloat16* __restrict__ out2,
@@ -216,7 +219,13 @@ __global__ void __launch_bounds__(kSepThreads, 1)
   // persistent: X of the next item may be loaded; the accumulators were read
   const uint32_t x_free = s_full + 64;
   const uint32_t acc_empty = s_full + 72;
-  static_assert(1 + 2 * kStages + 10 <= L::NBAR, "barrier region holds every barrier");
+  // dense non-persistent kernels: the output tile is staged in the X region
+  // (free once the last T GEMMs have run) and written by TMA stores that the
+  // producer lane issues; one round holds both sets' bf16 rows, or one set's
+  // fp32 partial rows
+  const uint32_t ep_full = s_full + 80, ep_empty = s_full + 88;
+  static_assert(1 + 2 * kStages + 12 <= L::NBAR, "barrier region holds every barrier");
+  constexpr bool kTmaOut = !PACKED && !PERSIST;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
   volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
@@ -236,7 +245,8 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       lay_ok = check_bar(ck, x_full, __LINE__) && check_bar(ck, s_full, __LINE__) &&
                check_bar(ck, s_free, __LINE__) && check_bar(ck, acc_full, __LINE__) &&
                check_bar(ck, drain, __LINE__) && check_bar(ck, x_free, __LINE__) &&
-               check_bar(ck, acc_empty, __LINE__);
+               check_bar(ck, acc_empty, __LINE__) && check_bar(ck, ep_full, __LINE__) &&
+               check_bar(ck, ep_empty, __LINE__);
       for (int s = 0; s < kStages; ++s)
         lay_ok = lay_ok && check_bar(ck, y_full(s), __LINE__) && check_bar(ck, y_empty(s), __LINE__);
       for (int b = 0; b < 2; ++b)
@@ -258,6 +268,8 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       mbar_init(drain, 2);  // one commit per MMA-issuing thread
       mbar_init(x_free, 1);
       mbar_init(acc_empty, kSoftmaxWarps);
+      mbar_init(ep_full, kSoftmaxWarps);
+      mbar_init(ep_empty, 1);
     }
     // a failure recorded earlier (this launch or a previous one), or a
     // failed layout check, skips the work
@@ -390,6 +402,33 @@ __global__ void __launch_bounds__(kSepThreads, 1)
       if (n_x > 0) wait_drain(x_full, (n_x - 1) & 1, timeout_ns);
       for (int j = max(0, g - kStages); j < g; ++j)
         wait_drain(y_full(j % kStages), (j / kStages) & 1, timeout_ns);
+    }
+    // output tiles staged by the softmax warps -> global memory
+    if (kTmaOut && lane == 0 && ok && item_steps(I0) > 0) {
+      const int rounds = split_out ? L::NSETS : 1;
+      for (int rd = 0; rd < rounds; ++rd) {
+        if (!wait_bounded(ep_full, rd & 1, wc)) break;
+        if (!dcheck(ck, I0.x0 < I0.NX && I0.sv.z < n_bh, __LINE__)) break;
+        if (split_out) {  // one set's fp32 rows: D/32 boxes of 16 KB
+#pragma unroll
+          for (int b = 0; b < D / 32; ++b)
+            tma_store_4d(&tm_o2, sb + L::OFF_X + b * 16384, b * 32, I0.x0, I0.sv.z,
+                         rd * splits + static_cast<int>(blockIdx.z));
+        } else {  // both sets' bf16 rows: D/64 boxes of 16 KB per set
+#pragma unroll
+          for (int t = 0; t < L::NSETS; ++t)
+#pragma unroll
+            for (int b = 0; b < D / 64; ++b)
+              tma_store_3d((HAS2 && t == 0) ? &tm_o2 : &tm_o1,
+                           sb + L::OFF_X + t * L::XT + b * 16384, b * 64, I0.x0, I0.sv.z);
+        }
+        bulk_commit_group();
+        if (rd + 1 < rounds) {
+          bulk_wait_read_all();  // the staging may be written again
+          mbar_arrive(ep_empty);
+        }
+      }
+      bulk_wait_all();  // the outputs are in global memory before the CTA exits
     }
   } else if (warp == 1 || warp == kGradWarp) {
     // ------------------------------------------------------------ MMA issuers
@@ -682,7 +721,51 @@ __global__ void __launch_bounds__(kSepThreads, 1)
         }
       }
     }
-    if (ok && n_iter > 0 && __all_sync(0xffffffffu, wait_bounded(acc_full, ic & 1, wc))) {
+    if (kTmaOut && ok && n_iter > 0 && __all_sync(0xffffffffu, wait_bounded(acc_full, ic & 1, wc))) {
+      tc_fence_after();
+      // row r's piece of EC columns into the staging tile: bf16 rows of set t
+      // at t XT, or (key split) one set's fp32 rows per round; 128-byte rows
+      // per 16 KB box, 16-byte chunks swizzled by the row
+      const bool f32 = split_out;
+      const int pb = EC * (f32 ? 4 : 2);        // bytes of this thread's piece
+      const int ppb = 128 / pb;                 // pieces per 128-byte box row
+      const uint32_t rowoff = static_cast<uint32_t>((grp / ppb) * 16384 + r * 128);
+      const int c0 = (grp % ppb) * (pb / 16);
+#pragma unroll
+      for (int t = 0; t < L::NSETS; ++t) {
+        float v[EC];
+        if (!(ok = check_tmem(ck, tmem + lane_off + L::COL_ACC + t * D + grp * EC, 32, EC, __LINE__)))
+          break;
+        if constexpr (EC == 32)
+          tmem_ld32(tmem + lane_off + L::COL_ACC + t * D + grp * EC, v);
+        else
+          tmem_ld16(tmem + lane_off + L::COL_ACC + t * D + grp * EC, v);
+        tmem_wait_ld();
+        if (f32) {
+          // round t: the producer has sent round t-1 out
+          if (t > 0 && !(ok = __all_sync(0xffffffffu, wait_bounded(ep_empty, (t - 1) & 1, wc)))) break;
+          const uint32_t base = sb + L::OFF_X + rowoff;
+#pragma unroll
+          for (int j = 0; j < EC / 4; ++j)
+            st_shared_v4(base + (((c0 + j) ^ (r & 7)) << 4), __float_as_uint(v[4 * j]),
+                         __float_as_uint(v[4 * j + 1]), __float_as_uint(v[4 * j + 2]),
+                         __float_as_uint(v[4 * j + 3]));
+        } else {
+          const uint32_t base = sb + L::OFF_X + t * L::XT + rowoff;
+#pragma unroll
+          for (int j = 0; j < EC / 8; ++j)
+            st_shared_v4(base + (((c0 + j) ^ (r & 7)) << 4), pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                         pack_bf16x2(v[8 * j + 2], v[8 * j + 3]), pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                         pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+        }
+        if (f32 || t + 1 == L::NSETS) {  // a round is complete
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ep_full);
+        }
+      }
+    } else if (!kTmaOut && ok && n_iter > 0 &&
+               __all_sync(0xffffffffu, wait_bounded(acc_full, ic & 1, wc))) {
       tc_fence_after();
 #pragma unroll
       for (int t = 0; t < L::NSETS; ++t) {
@@ -774,8 +857,17 @@ cudaError_t launch_sep_p(const BwdSepArgs& a, cudaStream_t stream) {
   const CUtensorMap* x2 = DQ ? a.tm_q2 : a.tm_k2;
   const CUtensorMap* y1 = DQ ? a.tm_k1 : a.tm_q1;
   const CUtensorMap* y2 = DQ ? a.tm_k2 : a.tm_q2;
+  // output maps of the dense non-persistent kernels (the others store rows
+  // directly and get the input maps as placeholders)
+  const CUtensorMap* o2 = x1;
+  const CUtensorMap* o1 = x1;
+  if (!PACKED && !PERSIST) {
+    o2 = splits > 1 ? a.tm_part : (DQ ? a.tm_dq2 : a.tm_dk2);
+    o1 = splits > 1 ? a.tm_part : (DQ ? a.tm_dq1 : a.tm_dk1);
+    if (o2 == nullptr || o1 == nullptr) return cudaErrorInvalidValue;
+  }
   kern<<<grid, kSepThreads, L::ALLOC, stream>>>(
-      *x1, *x2, *y1, *y2, a.NQ, a.NK, a.causal, a.scale, a.kl, a.lse1, a.lse2, a.g,
+      *x1, *x2, *y1, *y2, *o2, *o1, a.NQ, a.NK, a.causal, a.scale, a.kl, a.lse1, a.lse2, a.g,
       static_cast<__nv_bfloat16*>(DQ ? a.dq2 : a.dk2),
       static_cast<__nv_bfloat16*>(DQ ? a.dq1 : a.dk1), splits > 1 ? a.dq_part : nullptr, splits,
       a.dq_split_steps, a.BH, a.cu_q, a.cu_k, a.H, a.total_q, a.total_k, a.dev_status,

@@ -138,6 +138,15 @@ struct BwdSepArgs {
   // items (dense batches; 0: one CTA per key block)
   int dk_persist_ctas = 0;
   float* dq_part = nullptr;
+  // output tensor maps (dense batches; packed batches and the persistent dK
+  // kernel store rows directly): bf16 dK / dQ as {d, N, BH} with 64-column x
+  // 128-row boxes, the dQ split's fp32 partials as {d, N_Q, BH, set x split}
+  // with 32-column x 128-row boxes; a set not computed may repeat another map
+  const CUtensorMap* tm_dk2 = nullptr;
+  const CUtensorMap* tm_dk1 = nullptr;
+  const CUtensorMap* tm_dq2 = nullptr;
+  const CUtensorMap* tm_dq1 = nullptr;
+  const CUtensorMap* tm_part = nullptr;
   int* dev_status;
   uint64_t timeout_ns;
 };
