@@ -266,12 +266,13 @@ void dq_split_plan(int B, int H, int NQ, int NK, int d, int nsets, int* splits, 
   *splits = (steps + *per - 1) / *per;
 }
 
-// Persistent dK kernel for short query sweeps: with at most 8 steps of 64
-// query rows per key block (N_Q <= 512) a CTA's fixed start and end (X load,
+// Persistent dK kernel for short query sweeps: with at most 6 steps of 64
+// query rows per key block (N_Q <= 384) a CTA's fixed start and end (X load,
 // barrier and TMEM set-up, accumulator read-out) weigh against its few steps,
 // so one CTA per SM takes (key block, batch-head) items in turn and loads the
 // next item's X while the current one finishes. Measured on GB300 (64K-131K
-// keys): 1.25x at 64 query rows, 1.08x at 256, 1.01x at 512, 0.96x at 1024.
+// keys, against one CTA per key block writing its rows with TMA stores):
+// 1.11-1.18x at 128 query rows, 1.04x at 256, 1.01x at 384, 0.98-0.99x at 512.
 std::atomic<int> g_forced_dk_persist{0};  // 0: automatic, -1: never, n > 0: n CTAs
 
 int dk_persist_ctas(int B, int H, int NQ, int NK) {
@@ -280,7 +281,7 @@ int dk_persist_ctas(int B, int H, int NQ, int NK) {
   if (forced > 0) return forced;
   const long long items = static_cast<long long>((NK + skl::kBlockM - 1) / skl::kBlockM) * B * H;
   const int sms = num_sms();
-  return (NQ <= 512 && items > sms) ? sms : 0;
+  return (NQ <= 384 && items > sms) ? sms : 0;
 }
 
 size_t dq_split_ws(int B, int H, int NQ, int NK, int d, int nsets) {

@@ -146,7 +146,7 @@ int streamkl_set_bwd_dq_splits(int splits);
 
 /*
  * Persistent dK kernel of the separate algorithm for short query sweeps
- * (N_Q <= 512, dense batches, more (key block, batch-head) items than SMs):
+ * (N_Q <= 384, dense batches, more (key block, batch-head) items than SMs):
  * one CTA per SM takes the items in turn, heavy key blocks first, and loads
  * the next item's key block while the current one finishes, instead of one
  * CTA per key block paying its start and end each time. No counterpart in

@@ -139,12 +139,14 @@ def sweep_dqsplit(reps: int):
         res = {}
         for forced in (1, None):
             binding.set_bwd_dq_splits(forced)
+            binding.set_bwd_algorithm(binding.BWD_SEPARATE)  # 64 rows would go to the fused kernel
             try:
                 res[forced] = _time(lambda: binding.streamkl_bwd(
                     q1, k1, q2, k2, kl, l1, l2, g, w.scale, w.causal, grad1=w.grad1,
                     dev_status=st), reps)
             finally:
                 binding.set_bwd_dq_splits(None)
+                binding.set_bwd_algorithm(None)
         _check(st, w.name)
         s = binding.bwd_dq_splits(w.B, w.H, w.NQ, w.NK, w.d, w.causal, w.grad1)
         print(f"| {w.name} (B{w.B} H{w.H} {w.NQ}x{w.NK} d{w.d} causal) | "
@@ -171,12 +173,14 @@ def sweep_dkpersist(reps: int):
         res = {}
         for forced in (-1, None):
             binding.set_bwd_dk_persist(forced)
+            binding.set_bwd_algorithm(binding.BWD_SEPARATE)  # 64 rows would go to the fused kernel
             try:
                 res[forced] = _time(lambda: binding.streamkl_bwd(
                     q1, k1, q2, k2, kl, l1, l2, g, w.scale, w.causal, grad1=w.grad1,
                     dev_status=st), reps)
             finally:
                 binding.set_bwd_dk_persist(None)
+                binding.set_bwd_algorithm(None)
         _check(st, w.name)
         c = binding.bwd_dk_persist(w.B, w.H, w.NQ, w.NK, w.d, w.causal)
         print(f"| {w.name} (B{w.B} H{w.H} {w.NQ}x{w.NK} d{w.d} causal) | "

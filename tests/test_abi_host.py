@@ -199,13 +199,15 @@ def test_dq_key_split_choice(lib):
 
 
 def test_persistent_dk_choice(lib):
-    """The persistent dK kernel is used for short query sweeps (N_Q <= 512)
+    """The persistent dK kernel is used for short query sweeps (N_Q <= 384)
     with more (key block, batch-head) items than SMs, one CTA per SM; the
     override forces or disables it."""
     lib.streamkl_set_bwd_dk_persist(0)
-    sms = lib.streamkl_bwd_dk_persist(4, 32, 512, 131072, 128, 1)
+    sms = lib.streamkl_bwd_dk_persist(4, 32, 384, 131072, 128, 1)
     assert sms > 0  # 1024 key blocks x 128 slices
     assert lib.streamkl_bwd_dk_persist(4, 32, 64, 65536, 128, 1) == sms
+    # 8 query steps per key block (the split-K shape): one CTA per key block
+    assert lib.streamkl_bwd_dk_persist(4, 32, 512, 131072, 128, 1) == 0
     assert lib.streamkl_bwd_dk_persist(4, 32, 1024, 65536, 128, 1) == 0
     assert lib.streamkl_bwd_dk_persist(1, 32, 65536, 65536, 128, 1) == 0
     assert lib.streamkl_bwd_dk_persist(1, 1, 512, 512, 64, 0) == 0  # 4 items: fewer than SMs
@@ -214,7 +216,7 @@ def test_persistent_dk_choice(lib):
         assert lib.streamkl_set_bwd_dk_persist(3) == 0
         assert lib.streamkl_bwd_dk_persist(1, 32, 65536, 65536, 128, 1) == 3
         assert lib.streamkl_set_bwd_dk_persist(-1) == 0
-        assert lib.streamkl_bwd_dk_persist(4, 32, 512, 131072, 128, 1) == 0
+        assert lib.streamkl_bwd_dk_persist(4, 32, 384, 131072, 128, 1) == 0
         assert lib.streamkl_set_bwd_dk_persist(-2) == -1
     finally:
         lib.streamkl_set_bwd_dk_persist(0)
