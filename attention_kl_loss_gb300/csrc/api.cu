@@ -172,21 +172,25 @@ int forced_algo() {
 }
 
 // The fused algorithm runs the short-sweep kernel (persistent grid, dQ kept
-// on chip per batch-head) when the query rows fit one 64-row tile at d = 128,
-// and the kernel with one CTA per key tile and per-tile dQ reductions
-// otherwise.
+// on chip per batch-head) when the query rows fit one 64-row tile at d = 128;
+// otherwise one CTA per key tile, with per-tile dQ reductions (at d = 64
+// through TMA bulk reductions of staged tiles).
 bool short_sweep(int NQ, int d) { return d == 128 && NQ <= skl::kShortMaxQ; }
 
 // Automatic choice, from the fused-vs-separate sweep on GB300: the fused
 // short-sweep kernel for decode-like shapes (at most 64 query rows at
 // d = 128, where it reads the keys once against the separate kernels'
-// twice), the separate kernels everywhere else (at least as fast as the
-// per-key-tile fused kernel on every other shape measured).
+// twice); the fused d = 64 kernel with one gradient set from 512 query rows
+// on (1.02-1.33x: the separate kernels each pay the exponentials and dS that
+// bound d = 64, the fused kernel once; below 512 rows a CTA has only one to
+// three query blocks and the persistent dK kernel wins); the separate kernels
+// everywhere else.
 int bwd_algo_impl(int B, int H, int NQ, int NK, int d, int grad1) {
   const int forced = forced_algo();
   if (forced >= 0) return forced;
-  (void)B, (void)H, (void)NK, (void)grad1;
-  return short_sweep(NQ, d) ? 1 : 0;
+  (void)B, (void)H, (void)NK;
+  if (short_sweep(NQ, d)) return 1;
+  return (d == 64 && !grad1 && NQ >= 512) ? 1 : 0;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -306,6 +310,23 @@ streamkl_status make_map(CUtensorMap* m, const void* ptr, int BH, int N, int d, 
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(STREAMKL_ERR_CUDA, "tensor map for %s failed (CUresult %d)", name, static_cast<int>(r));
+  return STREAMKL_OK;
+}
+
+// 3-D map {d, N, BH} of an fp32 [BH][N][d] accumulator: 32-column (128-byte)
+// x 128-row boxes, 128-byte swizzle (the d = 64 fused kernel's TMA reductions).
+streamkl_status make_map_acc(CUtensorMap* m, void* ptr, int BH, int N, int d) {
+  auto enc = encode_fn();
+  if (!enc) return fail(STREAMKL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(skl::kBlockM), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, gdim, gstride, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(STREAMKL_ERR_CUDA, "tensor map for the dQ accumulator failed (CUresult %d)", static_cast<int>(r));
   return STREAMKL_OK;
 }
 
@@ -810,7 +831,23 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   a.dk1 = dk1;
   a.dev_status = dev_status;
   a.timeout_ns = wait_timeout_ns();
-  e = skl::launch_bwd(a, s);
+  if (d == 64) {
+    // one CTA per key tile; dQ through TMA reductions, dK through TMA stores
+    CUtensorMap mq2acc, mq1acc, mdk2, mdk1;
+    if ((st = make_map_acc(&mq2acc, a.dq2acc, BH, NQ, d)) != STREAMKL_OK) return st;
+    if ((st = make_map(&mdk2, dk2, BH, NK, d, "dk2", skl::kBlockN)) != STREAMKL_OK) return st;
+    if (grad1) {
+      if ((st = make_map_acc(&mq1acc, a.dq1acc, BH, NQ, d)) != STREAMKL_OK) return st;
+      if ((st = make_map(&mdk1, dk1, BH, NK, d, "dk1", skl::kBlockN)) != STREAMKL_OK) return st;
+    }
+    a.tm_dq2 = &mq2acc;
+    a.tm_dq1 = grad1 ? &mq1acc : &mq2acc;
+    a.tm_dk2 = &mdk2;
+    a.tm_dk1 = grad1 ? &mdk1 : &mdk2;
+    e = skl::launch_bwd_fused64(a, s);
+  } else {
+    e = skl::launch_bwd(a, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   e = skl::launch_dq_convert(a.dq2acc, dq2, n, s);
   if (e != cudaSuccess) return cuda_fail(e, "dq2 convert launch");

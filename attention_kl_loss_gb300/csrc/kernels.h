@@ -107,6 +107,14 @@ struct BwdArgs {
   float* dq1acc;  // same, grad1 only
   void* dk2;      // bf16 [BH][NK][d]
   void* dk1;      // bf16, grad1 only
+  // d = 64 kernel: the fp32 dQ accumulators as {d, N_Q, BH} maps with
+  // 32-column x 128-row boxes (TMA reductions) and the bf16 dK outputs as
+  // {d, N_K, BH} maps with 64-column x 128-row boxes (TMA stores); a set not
+  // computed may repeat the other's map
+  const CUtensorMap* tm_dq2 = nullptr;
+  const CUtensorMap* tm_dq1 = nullptr;
+  const CUtensorMap* tm_dk2 = nullptr;
+  const CUtensorMap* tm_dk1 = nullptr;
   int* dev_status;
   uint64_t timeout_ns;
 };
@@ -184,6 +192,8 @@ cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 bool fwd_pair_eligible(int NQ, int splits, bool packed);
 cudaError_t launch_fwd_combine(const FwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+// fused algorithm at d = 64 (one CTA per key tile, dQ through TMA reductions)
+cudaError_t launch_bwd_fused64(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_separate(const BwdSepArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_short(const BwdShortArgs& a, cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* acc, void* out_bf16, long long n, cudaStream_t stream);

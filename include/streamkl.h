@@ -107,10 +107,16 @@ int streamkl_set_fwd_pairs(int mode);
  *   0 = separate dK and dQ kernels: each keeps its accumulators on chip for
  *       its whole sweep; no atomics; a workspace only for the dQ kernel's
  *       key split (below);
- *   1 = one fused kernel per key tile: dK on chip, dQ reduced into an fp32
- *       workspace with global atomics, then converted to bf16.
- * The automatic choice is 0: on GB300 the separate kernels measured at least
- * as fast on every shape tried; 1 only when forced (below). Returns -1 on
+ *   1 = fused: every (query, key) pair visited once, dK on chip, dQ summed
+ *       into an fp32 workspace, then converted to bf16. At most 64 query
+ *       rows at d = 128: a persistent kernel over (batch-head, key tile)
+ *       items keeping dQ on chip per batch-head; at d = 64: one CTA per key
+ *       tile adding each query block's dQ with TMA bulk reductions; otherwise
+ *       one CTA per key tile with fp32 global reductions.
+ * The automatic choice (from the fused-vs-separate sweep on GB300) is 1 for
+ * at most 64 query rows at d = 128, and for d = 64 with one gradient set
+ * (want_grad1 = 0) and at least 512 query rows; 0 otherwise. Configuration 2
+ * alone runs 0 except at most 64 query rows at d = 128. Returns -1 on
  * invalid sizes.
  */
 int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int want_grad1);

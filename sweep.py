@@ -56,8 +56,9 @@ def _check(status, where):
 
 def sweep_algo(reps: int):
     """The fused algorithm (at most 64 query rows at d = 128: the short-sweep
-    kernel with dQ kept on chip per batch-head; otherwise one CTA per key tile
-    with dQ through fp32 L2 reductions) against the separate dK/dQ kernels."""
+    kernel with dQ kept on chip per batch-head; at d = 64 one CTA per key tile
+    with dQ through TMA reductions; otherwise one CTA per key tile with dQ
+    through fp32 L2 reductions) against the separate dK/dQ kernels."""
     dev = torch.device("cuda")
     shapes = [synthetic.WORKLOADS[n] for n in ("mid", "stress", "splitk", "causal64k")] + [
         synthetic.custom("decode64", B=4, H=32, NQ=64, NK=65536, d=128, causal=True, noise=0.1),
@@ -74,7 +75,15 @@ def sweep_algo(reps: int):
                          grad1=True),
     ] + [synthetic.custom(f"short{nq}x{nk // 1024}k", B=4, H=32, NQ=nq, NK=nk, d=128, causal=True,
                           noise=0.1)
-         for nq in (256, 1024, 2048) for nk in (65536, 131072)]
+         for nq in (256, 1024, 2048) for nk in (65536, 131072)] + [
+        # d = 64, one gradient set: the fused kernel with dQ through TMA reductions
+        synthetic.custom(f"d64_{nq}x{nk // 1024}k", B=b, H=h, NQ=nq, NK=nk, d=64, causal=causal,
+                         noise=0.2)
+        for (b, h, nq, nk, causal) in [(4, 32, 64, 65536, True), (4, 32, 128, 65536, True),
+                                       (4, 32, 256, 65536, True), (1, 8, 512, 131072, True),
+                                       (2, 16, 1024, 1024, False), (2, 16, 2048, 2048, True),
+                                       (2, 16, 4096, 4096, False), (1, 16, 16384, 16384, True),
+                                       (1, 8, 65536, 65536, True)]]
     print("| workload | sets | separate ms | fused ms | faster | library's choice |")
     print("|---|---|---:|---:|---|---|")
     for w in shapes:

@@ -361,6 +361,17 @@ SHORT = [
 ]
 
 
+@pytest.mark.parametrize("NQ,NK,causal", [(640, 777, True), (513, 1000, False), (1024, 1024, True)])
+def test_fused_d64_backward_automatic(NQ, NK, causal):
+    """At d = 64 with one gradient set and at least 512 query rows the library
+    picks the fused kernel (one CTA per key tile, dQ through TMA bulk
+    reductions of staged tiles): ragged shapes against the oracle."""
+    w = synthetic.custom(f"fused64_{NQ}x{NK}", B=2, H=2, NQ=NQ, NK=NK, d=64, causal=causal,
+                         noise=0.4, grad1=False)
+    assert binding.bwd_algorithm(w.B, w.H, w.NQ, w.NK, w.d, w.causal, False) == binding.BWD_FUSED
+    full_check(w, seed=NQ + NK, grad1=False)
+
+
 @pytest.mark.parametrize("B,H,NQ,NK,causal,sets", SHORT)
 def test_short_sweep_fused_backward(B, H, NQ, NK, causal, sets):
     """The fused algorithm's short-sweep kernel (at most 64 query rows, d =
