@@ -181,7 +181,7 @@ bool short_sweep(int NQ, int d) { return d == 128 && NQ <= skl::kShortMaxQ; }
 // short-sweep kernel for decode-like shapes (at most 64 query rows at
 // d = 128, where it reads the keys once against the separate kernels'
 // twice); the fused d = 64 kernel with one gradient set from 512 query rows
-// on (1.02-1.33x: the separate kernels each pay the exponentials and dS that
+// on (1.09-1.38x: the separate kernels each pay the exponentials and dS that
 // bound d = 64, the fused kernel once; below 512 rows a CTA has only one to
 // three query blocks and the persistent dK kernel wins); the separate kernels
 // everywhere else.

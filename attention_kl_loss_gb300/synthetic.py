@@ -79,6 +79,10 @@ WORKLOADS = {
         # a decode-like shape (64 query rows against 64K keys) on 8 heads, for
         # profiler captures of the fused short-sweep backward (keys 268 MB)
         Workload("decode_profile", B=1, H=8, NQ=64, NK=65536, d=128, causal=True, noise=0.1),
+        # d = 64, one gradient set, causal 16K on 16 heads (inputs 134 MB, above
+        # L2): profiler captures of the fused d = 64 backward
+        Workload("causal16k_d64_profile", B=1, H=16, NQ=16384, NK=16384, d=64, causal=True,
+                 noise=0.2),
     ]
 }
 
