@@ -23,7 +23,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_NAME = "libstreamkl.so"
 DEBUG_LIB_NAME = "libstreamkl_debug.so"
-SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_sep.cu", "bwd_short.cu", "bwd_fused.cu"]
+SOURCES = ["api.cu", "fwd.cu", "bwd.cu", "bwd_sep.cu", "bwd_short.cu", "bwd_fused.cu", "bwd_fused128.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]

@@ -314,14 +314,15 @@ streamkl_status make_map(CUtensorMap* m, const void* ptr, int BH, int N, int d, 
 }
 
 // 3-D map {d, N, BH} of an fp32 [BH][N][d] accumulator: 32-column (128-byte)
-// x 128-row boxes, 128-byte swizzle (the d = 64 fused kernel's TMA reductions).
-streamkl_status make_map_acc(CUtensorMap* m, void* ptr, int BH, int N, int d) {
+// x box_rows boxes, 128-byte swizzle (the fused kernels' TMA reductions).
+streamkl_status make_map_acc(CUtensorMap* m, void* ptr, int BH, int N, int d,
+                             int box_rows = skl::kBlockM) {
   auto enc = encode_fn();
   if (!enc) return fail(STREAMKL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
   const cuuint64_t gdim[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(BH)};
   const cuuint64_t gstride[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
-  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(skl::kBlockM), 1};
+  const cuuint32_t box[3] = {32, static_cast<cuuint32_t>(box_rows), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, gdim, gstride, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -846,7 +847,23 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
     a.tm_dk1 = grad1 ? &mdk1 : &mdk2;
     e = skl::launch_bwd_fused64(a, s);
   } else {
-    e = skl::launch_bwd(a, s);
+    // 64-row query steps: Q maps with 64-row boxes; dQ^T through TMA reductions
+    CUtensorMap mq1s, mq2s, mq2acc, mq1acc, mdk2, mdk1;
+    if ((st = make_map(&mq1s, q1, BH, NQ, d, "q1", 64)) != STREAMKL_OK) return st;
+    if ((st = make_map(&mq2s, q2, BH, NQ, d, "q2", 64)) != STREAMKL_OK) return st;
+    if ((st = make_map_acc(&mq2acc, a.dq2acc, BH, NQ, d, 64)) != STREAMKL_OK) return st;
+    if ((st = make_map(&mdk2, dk2, BH, NK, d, "dk2", skl::kBlockN)) != STREAMKL_OK) return st;
+    if (grad1) {
+      if ((st = make_map_acc(&mq1acc, a.dq1acc, BH, NQ, d, 64)) != STREAMKL_OK) return st;
+      if ((st = make_map(&mdk1, dk1, BH, NK, d, "dk1", skl::kBlockN)) != STREAMKL_OK) return st;
+    }
+    a.tm_q1 = &mq1s;
+    a.tm_q2 = &mq2s;
+    a.tm_dq2 = &mq2acc;
+    a.tm_dq1 = grad1 ? &mq1acc : &mq2acc;
+    a.tm_dk2 = &mdk2;
+    a.tm_dk1 = grad1 ? &mdk1 : &mdk2;
+    e = skl::launch_bwd_fused128(a, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   e = skl::launch_dq_convert(a.dq2acc, dq2, n, s);

@@ -92,6 +92,8 @@ struct FwdArgs {
   uint64_t timeout_ns;
 };
 
+// Fused algorithm beyond the short-sweep shapes (one CTA per key tile, each
+// (query, key) pair visited once, dQ added into fp32 accumulators).
 struct BwdArgs {
   const CUtensorMap* tm_q1;
   const CUtensorMap* tm_k1;
@@ -103,7 +105,7 @@ struct BwdArgs {
   const float* lse1;
   const float* lse2;
   const float* g;
-  float* dq2acc;  // [BH][NQ][d] fp32, zeroed by the caller of launch_bwd
+  float* dq2acc;  // [BH][NQ][d] fp32, zeroed by the caller
   float* dq1acc;  // same, grad1 only
   void* dk2;      // bf16 [BH][NK][d]
   void* dk1;      // bf16, grad1 only
@@ -191,9 +193,12 @@ constexpr int kShortMaxQ = 64;  // query rows the short-sweep kernel handles
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
 bool fwd_pair_eligible(int NQ, int splits, bool packed);
 cudaError_t launch_fwd_combine(const FwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
 // fused algorithm at d = 64 (one CTA per key tile, dQ through TMA reductions)
 cudaError_t launch_bwd_fused64(const BwdArgs& a, cudaStream_t stream);
+// fused algorithm at d = 128: one CTA per key tile, 64-row query steps, dQ^T
+// through TMA reductions; the Q maps with 64-row boxes, the dQ accumulator
+// maps with 32-column x 64-row boxes
+cudaError_t launch_bwd_fused128(const BwdArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_separate(const BwdSepArgs& a, cudaStream_t stream);
 cudaError_t launch_bwd_short(const BwdShortArgs& a, cudaStream_t stream);
 cudaError_t launch_dq_convert(const float* acc, void* out_bf16, long long n, cudaStream_t stream);
@@ -201,7 +206,6 @@ cudaError_t launch_wait_selftest(int* dev_status, uint64_t timeout_ns, cudaStrea
 cudaError_t launch_check_selftest(int* dev_status, cudaStream_t stream);
 
 size_t fwd_smem_bytes(int d);
-size_t bwd_smem_bytes(int d, int grad1);
 size_t bwd_sep_smem_bytes(int d, int grad1);
 size_t bwd_short_smem_bytes(int grad1, int grad2);
 

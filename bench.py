@@ -547,13 +547,15 @@ def gpu_arm(args, w):
                     "regenerates S1 and S2, so they execute 16d FLOPs per pair with both "
                     "gradient sets against the method's 12d")
     elif NQ <= 64 and d == 128:
-        bwd_name = "streamkl_bwd_kernel"
-        bwd_note = ("fused algorithm, short-sweep kernel (streamkl_bwd_short_kernel: each pair "
-                    "visited once, dQ kept on chip per batch-head); includes the workspace clear "
-                    "and the fp32->bf16 dQ conversion; bound by HBM")
+        bwd_name = "streamkl_bwd_short_kernel"
+        bwd_note = ("fused algorithm, short-sweep kernel (each pair visited once, dQ kept on chip "
+                    "per batch-head); includes the workspace clear and the fp32->bf16 dQ "
+                    "conversion; bound by HBM")
     else:
-        bwd_name = "streamkl_bwd_kernel"
-        bwd_note = "fused kernel; includes the workspace clear and the fp32->bf16 dQ conversion"
+        bwd_name = "streamkl_bwd_fused_kernel" if d == 64 else "streamkl_bwd_fused128_kernel"
+        bwd_note = ("fused algorithm, one CTA per key tile (each pair visited once, dQ added with "
+                    "TMA bulk reductions); includes the workspace clear and the fp32->bf16 dQ "
+                    "conversion")
     short_sweep = (not separate) and NQ <= 64 and d == 128
     step_flops = f_fwd + f_bwd_metric
     value = world * step_flops / (ms_step * 1e-3) / 1e12

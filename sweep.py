@@ -83,7 +83,17 @@ def sweep_algo(reps: int):
                                        (4, 32, 256, 65536, True), (1, 8, 512, 131072, True),
                                        (2, 16, 1024, 1024, False), (2, 16, 2048, 2048, True),
                                        (2, 16, 4096, 4096, False), (1, 16, 16384, 16384, True),
-                                       (1, 8, 65536, 65536, True)]]
+                                       (1, 8, 65536, 65536, True)]] + [
+        # d = 128, moderate key lengths: the fused kernel's dQ reductions against
+        # the separate kernels' second pass over the scores
+        synthetic.custom(f"d128_{nq}x{nk // 1024}k", B=b, H=h, NQ=nq, NK=nk, d=128, causal=causal,
+                         noise=0.2, grad1=g1)
+        for (b, h, nq, nk, causal, g1) in [(2, 16, 2048, 2048, False, False),
+                                           (4, 32, 2048, 2048, True, False),
+                                           (2, 16, 8192, 8192, False, False),
+                                           (1, 16, 16384, 16384, True, False),
+                                           (2, 16, 4096, 4096, False, True),
+                                           (4, 16, 2048, 8192, True, False)]]
     print("| workload | sets | separate ms | fused ms | faster | library's choice |")
     print("|---|---|---:|---:|---|---|")
     for w in shapes:
