@@ -60,12 +60,14 @@ def test_captured_step_replays_like_eager(NQ, NK, d, causal, grad1):
             assert torch.equal(a, b)
 
 
-# (name, shape): separate kernels, split forward with a workspace, and the
-# short-sweep fused backward (its dQ summed with fp32 reductions)
+# (name, shape): separate kernels, split forward with a workspace, the
+# short-sweep fused backward and the fused d = 64 backward (their dQ summed
+# with fp32 reductions)
 CASES = [
     ("separate", dict(B=2, H=3, NQ=300, NK=333, d=128, causal=True, grad1=True)),
     ("split forward d64", dict(B=1, H=4, NQ=64, NK=8192, d=64, causal=True)),
     ("short sweep", dict(B=2, H=8, NQ=48, NK=4000, d=128, causal=True, grad1=True)),
+    ("fused d64", dict(B=1, H=2, NQ=640, NK=700, d=64, causal=True)),
 ]
 
 
