@@ -183,14 +183,19 @@ bool short_sweep(int NQ, int d) { return d == 128 && NQ <= skl::kShortMaxQ; }
 // twice); the fused d = 64 kernel with one gradient set from 512 query rows
 // on (1.09-1.38x: the separate kernels each pay the exponentials and dS that
 // bound d = 64, the fused kernel once; below 512 rows a CTA has only one to
-// three query blocks and the persistent dK kernel wins); the separate kernels
-// everywhere else.
-int bwd_algo_impl(int B, int H, int NQ, int NK, int d, int grad1) {
+// three query blocks and the persistent dK kernel wins); the fused d = 128
+// kernel with one gradient set from 512 query rows on without a mask and from
+// 1,024 with the causal one (non-causal 1.02-1.12x, causal 1.00-1.02x; at 512
+// causal rows, the split-K shape, and at 256 rows the separate kernels are
+// faster); the separate kernels everywhere else, both gradient sets included.
+int bwd_algo_impl(int B, int H, int NQ, int NK, int d, int causal, int grad1) {
   const int forced = forced_algo();
   if (forced >= 0) return forced;
   (void)B, (void)H, (void)NK;
   if (short_sweep(NQ, d)) return 1;
-  return (d == 64 && !grad1 && NQ >= 512) ? 1 : 0;
+  if (grad1) return 0;
+  if (d == 64) return NQ >= 512 ? 1 : 0;
+  return NQ >= (causal ? 1024 : 512) ? 1 : 0;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -200,8 +205,8 @@ size_t fwd_ws(int B, int H, int NQ, int splits) {
   return align256(static_cast<size_t>(5) * splits * B * H * NQ * sizeof(float));
 }
 
-size_t bwd_ws(int B, int H, int NQ, int NK, int d, int grad1) {
-  if (bwd_algo_impl(B, H, NQ, NK, d, grad1) == 0) return 0;
+size_t bwd_ws(int B, int H, int NQ, int NK, int d, int causal, int grad1) {
+  if (bwd_algo_impl(B, H, NQ, NK, d, causal, grad1) == 0) return 0;
   const size_t one = align256(static_cast<size_t>(B) * H * NQ * d * sizeof(float));
   return grad1 ? 2 * one : one;
 }
@@ -432,8 +437,8 @@ size_t streamkl_bwd_workspace_size(int B, int H, int NQ, int NK, int d, int caus
   if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return 0;
   const int g1 = want_grad1 ? 1 : 0;
   const size_t sep = dq_split_ws(B, H, NQ, NK, d, 1 + g1);
-  if (bwd_algo_impl(B, H, NQ, NK, d, g1) == 0) return sep;
-  const size_t fused = bwd_ws(B, H, NQ, NK, d, g1);
+  if (bwd_algo_impl(B, H, NQ, NK, d, causal, g1) == 0) return sep;
+  const size_t fused = bwd_ws(B, H, NQ, NK, d, causal, g1);
   // one set under the per-key-tile fused algorithm may be configuration 2
   // alone, which that kernel hands to the separate kernels
   if (!g1 && !short_sweep(NQ, d)) return fused > sep ? fused : sep;
@@ -488,7 +493,7 @@ int streamkl_set_fwd_pairs(int mode) {
 
 int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int want_grad1) {
   if (check_sizes(B, H, NQ, NK, d, causal) != STREAMKL_OK) return -1;
-  return bwd_algo_impl(B, H, NQ, NK, d, want_grad1 ? 1 : 0);
+  return bwd_algo_impl(B, H, NQ, NK, d, causal, want_grad1 ? 1 : 0);
 }
 
 int streamkl_set_bwd_algorithm(int algo) {
@@ -688,14 +693,14 @@ streamkl_status streamkl_bwd(const void* q1, const void* k1, const void* q2, con
   // configuration 2 alone runs the separate kernels unless the fused
   // algorithm's short-sweep kernel takes the shape (the per-key-tile fused
   // kernel always produces dQ2/dK2)
-  int algo = bwd_algo_impl(B, H, NQ, NK, d, grad1);
+  int algo = bwd_algo_impl(B, H, NQ, NK, d, causal, grad1);
   if (!grad2 && !(algo == 1 && short_sweep(NQ, d))) algo = 0;
   // separate kernels: the dQ kernel's key split keeps its fp32 partials in
   // the workspace; fused kernels: one fp32 dQ accumulator per gradient set
   int dq_splits = 1, dq_per = 0;
   if (algo == 0) dq_split_plan(B, H, NQ, NK, d, grad1 + grad2, &dq_splits, &dq_per);
   const size_t need = algo == 0 ? dq_split_ws(B, H, NQ, NK, d, grad1 + grad2)
-                                : bwd_ws(B, H, NQ, NK, d, grad1 && grad2);
+                                : bwd_ws(B, H, NQ, NK, d, causal, grad1 && grad2);
   if (need > 0 && (!workspace || ws_bytes < need || !aligned16(workspace)))
     return fail(STREAMKL_ERR_INVALID_ARG, "backward workspace too small: need %zu bytes, got %zu", need, ws_bytes);
 

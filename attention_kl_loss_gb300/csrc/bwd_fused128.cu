@@ -20,6 +20,12 @@
 // stay below the work saved. dK leaves once at the end through the staging
 // tile and TMA stores.
 //
+// The kernel is bound by its step's dependency chain, not by one unit: a
+// tcgen05.mma of M = 128 costs ~45 cycles whatever N <= 64 (timed alone), so
+// the N = 64 GEMMs run at two thirds of the tensor rate at best. With one
+// gradient set the T GEMMs take K from TMEM (copied there once per CTA by the
+// softmax warps) and the freed K tile becomes a second dQ staging tile.
+//
 // Gradients of L = sum_i g_i KL_i, with s = scale * q.k (g and scale folded
 // into dS):
 //   configuration 1 (teacher P1 fixed):  dS2 = g * (P2 - P1)
@@ -33,13 +39,20 @@
 // g = (w-2)/4 (T: thread = key row, query columns [16g, 16g+16); dQ^T
 // read-out: thread = d column, queries [16g, 16g+16); dK read-out: thread =
 // key row, d columns [32g, 32g+32)); 18 = TMA reductions and stores (lane 0).
-// TMEM: T1 [0,64) T2 [64,128) | dK per set (128 columns) | dQ^T per set (64).
+// TMEM: T1 [0,64) T2 [64,128) | dK per set (128 columns) | dQ^T per set (64)
+// | one set: K1, K2 as packed bf16 pairs (64 columns each).
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace skl {
 
 namespace {
+
+// the bulk copy groups of this thread, but the most recent one, have finished
+// reading shared memory
+__device__ __forceinline__ void bulk_wait_read_le1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 
 constexpr int kF2Threads = 608;  // 19 warps
 constexpr int kF2SoftmaxWarps = 16;
@@ -59,22 +72,33 @@ struct Fused128Layout {
   static constexpr int STG = kF2Step * kF2D * 4;       // one set's fp32 dQ rows: 4 boxes of 8 KB
   static_assert(STG >= kBlockN * kF2D * 2, "the staging tile also holds one set's bf16 dK");
   static constexpr int TAB = 4 * kF2Step * 4;          // per stage: 4 x 64 floats
+  // one gradient set: K1, K2 also in TMEM (64 packed columns each), the A
+  // operand of the T GEMMs, which then read only Q from shared memory. The K
+  // tile that the dQ GEMMs do not read (K1 for configuration 1, K2 for
+  // configuration 2) is free after that copy and becomes a second staging
+  // tile, so that a step's dQ read-out does not wait for the previous step's
+  // reductions to leave shared memory.
+  static constexpr bool KTM = NSETS == 1;
+  static constexpr int NSTG = KTM ? 2 : 1;             // staging tiles
   static constexpr int OFF_K = 0;                      // K1, K2
+  static constexpr int OFF_STG1 = OFF_K + (SETS == kSet2 ? 0 : KT);  // second staging tile
   static constexpr int OFF_Q = 2 * KT;                 // stage s: Q1 at +2s QT, Q2 at +(2s+1) QT
   static constexpr int OFF_DS = OFF_Q + STAGES * 2 * QT;  // slot t: the t-th computed set
   static constexpr int OFF_STG = OFF_DS + NSETS * DST;
   static constexpr int OFF_TAB = OFF_STG + STG;
   static constexpr int OFF_BAR = OFF_TAB + STAGES * TAB;
   // k_full, q_full[S], q_empty[S], t_full, t_free, ds_full, ds_free, dq_full,
-  // dq_free, dk_full, stg_full, stg_empty, drain
-  static constexpr int NBAR = 1 + 2 * STAGES + 10;
+  // dq_free, dk_full, stg_full, stg_empty, drain, kt_full, then stg_full and
+  // stg_empty of staging tile 1
+  static constexpr int NBAR = 1 + 2 * STAGES + 13;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;
   static constexpr uint32_t COL_T = 0, COL_DK = 2 * kF2Step, COL_DQ = COL_DK + NSETS * kF2D;
-  static_assert(COL_DQ + NSETS * kF2Step <= 512, "TMEM budget");
+  static constexpr uint32_t COL_K = COL_DQ + NSETS * kF2Step;
+  static_assert(COL_K + (KTM ? kF2D : 0) <= 512, "TMEM budget");
   static_assert(ALLOC <= 232448, "shared memory budget");
-  static_assert(OFF_Q % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_STG % 1024 == 0,
+  static_assert(OFF_Q % 1024 == 0 && OFF_DS % 1024 == 0 && OFF_STG % 1024 == 0 && OFF_STG1 % 1024 == 0,
                 "swizzled tiles on 1024-byte boundaries");
 };
 
@@ -118,7 +142,14 @@ __global__ void __launch_bounds__(kF2Threads, 1)
   const uint32_t t_free = t_full + 8, ds_full = t_full + 16, ds_free = t_full + 24;
   const uint32_t dq_full = t_full + 32, dq_free = t_full + 40, dk_full = t_full + 48;
   const uint32_t stg_full = t_full + 56, stg_empty = t_full + 64, drain = t_full + 72;
-  static_assert(1 + 2 * L::STAGES + 10 == L::NBAR, "barrier region holds every barrier");
+  const uint32_t kt_full = t_full + 80;  // K rows copied into TMEM
+  static_assert(1 + 2 * L::STAGES + 13 == L::NBAR, "barrier region holds every barrier");
+  // staging use u (one per set and step, then one per set for dK) goes
+  // through tile u % NSTG
+  constexpr int NSTG = L::NSTG;
+  auto stg_full_b = [&](int u) { return u % NSTG ? t_full + 88 : stg_full; };
+  auto stg_empty_b = [&](int u) { return u % NSTG ? t_full + 96 : stg_empty; };
+  auto stg_tile = [&](int u) { return sb + (u % NSTG ? L::OFF_STG1 : L::OFF_STG); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
   volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
@@ -132,7 +163,7 @@ __global__ void __launch_bounds__(kF2Threads, 1)
     bool lay_ok = true;
     if (kDeviceChecks) {  // every barrier address inside the barrier region
       lay_ok = check_bar(ck, k_full, __LINE__) && check_bar(ck, t_full, __LINE__) &&
-               check_bar(ck, drain, __LINE__);
+               check_bar(ck, drain, __LINE__) && check_bar(ck, stg_empty_b(1), __LINE__);
       for (int s = 0; s < L::STAGES; ++s)
         lay_ok = lay_ok && check_bar(ck, q_full(s), __LINE__) && check_bar(ck, q_empty(s), __LINE__);
     }
@@ -152,6 +183,9 @@ __global__ void __launch_bounds__(kF2Threads, 1)
       mbar_init(stg_full, kF2SoftmaxWarps);
       mbar_init(stg_empty, 1);
       mbar_init(drain, 1);
+      mbar_init(kt_full, kF2SoftmaxWarps);
+      mbar_init(stg_full_b(1), kF2SoftmaxWarps);
+      mbar_init(stg_empty_b(1), 1);
     }
     // a failure recorded earlier (this launch or a previous one), or a
     // failed layout check, skips the work
@@ -257,13 +291,18 @@ __global__ void __launch_bounds__(kF2Threads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
+      // the whole of TMEM is this CTA's, so its base address is 0; a
+      // compile-time base keeps the MMA operand addresses constants
+      constexpr uint32_t tmem = 0;
       constexpr uint32_t id_t = idesc_bf16(kBlockN, STEP, 0, 0);  // T = K Q^T
       constexpr uint32_t id_dk = idesc_bf16(kBlockN, D, 0, 1);    // dK = dS Q
       constexpr uint32_t id_dq = idesc_bf16(D, STEP, 1, 1);       // dQ^T = K^T dS
       bool ok = check_tmem(ck, tmem + L::COL_T, 128, 2 * STEP, __LINE__) &&
                 check_tmem(ck, tmem + L::COL_DK, 128, L::NSETS * D, __LINE__) &&
                 check_tmem(ck, tmem + L::COL_DQ, 128, L::NSETS * STEP, __LINE__) &&
-                wait_bounded(k_full, 0, wc);
+                (!L::KTM || check_tmem(ck, tmem + L::COL_K, 128, D, __LINE__)) &&
+                dcheck(ck, *tmem_slot == 0u, __LINE__) &&
+                wait_bounded(k_full, 0, wc) && (!L::KTM || wait_bounded(kt_full, 0, wc));
       const uint32_t k1s = sb + L::OFF_K, k2s = k1s + L::KT;
       // T of step j: two K-major GEMMs (A = K tile, B = Q tile), k-steps interleaved
       auto issue_t = [&](int j) {
@@ -271,10 +310,17 @@ __global__ void __launch_bounds__(kF2Threads, 1)
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t ko = (k >> 2) * 16384 + (k & 3) * 32, qo = (k >> 2) * 8192 + (k & 3) * 32;
-          mma_bf16(tmem + L::COL_T, smem_desc_sw128(k1s + ko, 16, 1024),
-                   smem_desc_sw128(qs + qo, 16, 1024), id_t, k > 0);
-          mma_bf16(tmem + L::COL_T + STEP, smem_desc_sw128(k2s + ko, 16, 1024),
-                   smem_desc_sw128(qs + L::QT + qo, 16, 1024), id_t, k > 0);
+          if constexpr (L::KTM) {
+            mma_bf16_ts(tmem + L::COL_T, tmem + L::COL_K + 8 * k, smem_desc_sw128(qs + qo, 16, 1024), id_t,
+                        k > 0);
+            mma_bf16_ts(tmem + L::COL_T + STEP, tmem + L::COL_K + D / 2 + 8 * k,
+                        smem_desc_sw128(qs + L::QT + qo, 16, 1024), id_t, k > 0);
+          } else {
+            mma_bf16(tmem + L::COL_T, smem_desc_sw128(k1s + ko, 16, 1024),
+                     smem_desc_sw128(qs + qo, 16, 1024), id_t, k > 0);
+            mma_bf16(tmem + L::COL_T + STEP, smem_desc_sw128(k2s + ko, 16, 1024),
+                     smem_desc_sw128(qs + L::QT + qo, 16, 1024), id_t, k > 0);
+          }
         }
         mma_commit(t_full);
       };
@@ -344,30 +390,39 @@ __global__ void __launch_bounds__(kF2Threads, 1)
     if (lane == 0 && n > 0) {
       bool ok = true;
       int u = 0;  // staging uses so far
+      // after issuing the copies of use u: the tile of use u - (NSTG - 1) has
+      // been read (at most NSTG - 1 copy groups still reading) and may be
+      // written again
+      auto release_stage = [&](int uu) {
+        bulk_commit_group();
+        if constexpr (NSTG == 2) {
+          bulk_wait_read_le1();
+          if (uu >= 1) mbar_arrive(stg_empty_b(uu - 1));
+        } else {
+          bulk_wait_read_all();
+          mbar_arrive(stg_empty_b(uu));
+        }
+      };
       for (int j = 0; ok && j < n; ++j) {
         const int q0 = (qs0 + j) * STEP;
         for (int t = 0; t < L::NSETS; ++t, ++u) {
-          if (!(ok = wait_bounded(stg_full, u & 1, wc))) break;
+          if (!(ok = wait_bounded(stg_full_b(u), (u / NSTG) & 1, wc))) break;
           if (!(ok = dcheck(ck, q0 < NQ && bh < BH, __LINE__))) break;
           const CUtensorMap* m = (HAS2 && t == 0) ? &tm_dq2 : &tm_dq1;
           // rows past N_Q (the last step's tail) are not reduced into
 #pragma unroll
-          for (int b = 0; b < D / 32; ++b) tma_reduce_add_3d(m, sb + L::OFF_STG + b * 8192, b * 32, q0, bh);
-          bulk_commit_group();
-          bulk_wait_read_all();  // the staging tile may be written again
-          mbar_arrive(stg_empty);
+          for (int b = 0; b < D / 32; ++b) tma_reduce_add_3d(m, stg_tile(u) + b * 8192, b * 32, q0, bh);
+          release_stage(u);
         }
       }
       // dK rows of each set, through the same staging tile
       for (int t = 0; ok && t < L::NSETS; ++t, ++u) {
-        if (!(ok = wait_bounded(stg_full, u & 1, wc))) break;
+        if (!(ok = wait_bounded(stg_full_b(u), (u / NSTG) & 1, wc))) break;
         if (!(ok = dcheck(ck, k0 < NK && bh < BH, __LINE__))) break;
         const CUtensorMap* m = (HAS2 && t == 0) ? &tm_dk2 : &tm_dk1;
-        tma_store_3d(m, sb + L::OFF_STG, 0, k0, bh);
-        tma_store_3d(m, sb + L::OFF_STG + 16384, 64, k0, bh);
-        bulk_commit_group();
-        bulk_wait_read_all();
-        mbar_arrive(stg_empty);
+        tma_store_3d(m, stg_tile(u), 0, k0, bh);
+        tma_store_3d(m, stg_tile(u) + 16384, 64, k0, bh);
+        release_stage(u);
       }
       bulk_wait_all();  // every reduction and store is in global memory before the CTA exits
     }
@@ -382,9 +437,9 @@ __global__ void __launch_bounds__(kF2Threads, 1)
     const int qlo = causal ? key - off : 0;  // queries >= qlo see this key (all, when non-causal)
     bool ok = true;
     int u = 0;  // staging uses so far
-    // the staging tile is free again (the store warp has read use u-1)
+    // staging tile u % NSTG is free again (the store warp has read use u - NSTG)
     auto stage_free = [&]() {
-      return u == 0 || __all_sync(0xffffffffu, wait_bounded(stg_empty, (u - 1) & 1, wc));
+      return u < NSTG || __all_sync(0xffffffffu, wait_bounded(stg_empty_b(u), (u / NSTG - 1) & 1, wc));
     };
     // dQ^T of step j (thread = d column r, queries [16 grp, 16 grp + 16)) ->
     // staging rows q, fp32 (box r/32 of 32 columns x 64 rows, 4-byte slot r%32
@@ -392,7 +447,6 @@ __global__ void __launch_bounds__(kF2Threads, 1)
     auto read_dq = [&](int j) {
       if (!__all_sync(0xffffffffu, wait_bounded(dq_full, j & 1, wc))) return false;
       tc_fence_after();
-      const uint32_t col = sb + L::OFF_STG + static_cast<uint32_t>((r >> 5) * 8192);
       const int cb = (r & 31) * 4;  // byte of this column within a 128-byte row
 #pragma unroll
       for (int t = 0; t < L::NSETS; ++t, ++u) {
@@ -407,6 +461,7 @@ __global__ void __launch_bounds__(kF2Threads, 1)
           if (lane == 0) mbar_arrive(dq_free);
         }
         if (!stage_free()) return false;
+        const uint32_t col = stg_tile(u) + static_cast<uint32_t>((r >> 5) * 8192);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const int q = grp * 16 + k;
@@ -414,10 +469,32 @@ __global__ void __launch_bounds__(kF2Threads, 1)
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(stg_full);
+        if (lane == 0) mbar_arrive(stg_full_b(u));
       }
       return true;
     };
+    if constexpr (L::KTM) {
+      // K1, K2 row r into TMEM lane r: this thread's 32 d values of each (the
+      // 64-column box grp/2, 16-byte chunks 4 (grp%2) .. +4 of the swizzled
+      // row) -> packed columns [16 grp, +16)
+      if (n > 0 && (ok = __all_sync(0xffffffffu, wait_bounded(k_full, 0, wc)) &&
+                         check_tmem(ck, tmem + lane_off + L::COL_K + 16 * grp, 32, D / 2 + 16, __LINE__))) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t rowk = sb + L::OFF_K + t * L::KT + static_cast<uint32_t>((grp >> 1) * 16384 + r * 128);
+          uint32_t w[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            ld_shared_v4(rowk + (((4 * (grp & 1) + q) ^ (r & 7)) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                         w[4 * q + 3]);
+          tmem_st_cols<16>(tmem + lane_off + L::COL_K + t * (D / 2) + 16 * grp, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kt_full);
+      }
+    }
     for (int j = 0; ok && j < n; ++j) {
       const int s = j % L::STAGES;
       const int q0 = (qs0 + j) * STEP + grp * 16;  // this thread's first query column
@@ -507,9 +584,9 @@ __global__ void __launch_bounds__(kF2Threads, 1)
     // chunks 4 (grp%2) .. +4 of the row) -> the store warp's TMA stores
     if (ok && n > 0 && __all_sync(0xffffffffu, wait_bounded(dk_full, 0, wc))) {
       tc_fence_after();
-      const uint32_t row = sb + L::OFF_STG + static_cast<uint32_t>((grp >> 1) * 16384 + r * 128);
 #pragma unroll
       for (int t = 0; t < L::NSETS; ++t, ++u) {
+        const uint32_t row = stg_tile(u) + static_cast<uint32_t>((grp >> 1) * 16384 + r * 128);
         float v[32];
         if (!check_tmem(ck, tmem + lane_off + L::COL_DK + t * D + grp * 32, 32, 32, __LINE__)) break;
         tmem_ld32(tmem + lane_off + L::COL_DK + t * D + grp * 32, v);
@@ -522,7 +599,7 @@ __global__ void __launch_bounds__(kF2Threads, 1)
                        pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(stg_full);
+        if (lane == 0) mbar_arrive(stg_full_b(u));
       }
     }
   }

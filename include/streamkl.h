@@ -110,14 +110,15 @@ int streamkl_set_fwd_pairs(int mode);
  *   1 = fused: every (query, key) pair visited once, dK on chip, dQ summed
  *       into an fp32 workspace, then converted to bf16. At most 64 query
  *       rows at d = 128: a persistent kernel over (batch-head, key tile)
- *       items keeping dQ on chip per batch-head; at d = 64: one CTA per key
- *       tile adding each query block's dQ with TMA bulk reductions; otherwise
- *       one CTA per key tile with fp32 global reductions.
+ *       items keeping dQ on chip per batch-head; otherwise one CTA per key
+ *       tile adding each query block's dQ with TMA bulk reductions (128-row
+ *       blocks at d = 64, 64-row steps at d = 128).
  * The automatic choice (from the fused-vs-separate sweep on GB300) is 1 for
- * at most 64 query rows at d = 128, and for d = 64 with one gradient set
- * (want_grad1 = 0) and at least 512 query rows; 0 otherwise. Configuration 2
- * alone runs 0 except at most 64 query rows at d = 128. Returns -1 on
- * invalid sizes.
+ * at most 64 query rows at d = 128; with one gradient set (want_grad1 = 0)
+ * for at least 512 query rows at d = 64, and at d = 128 for at least 512
+ * query rows without the mask or 1,024 with causal = 1; 0 otherwise.
+ * Configuration 2 alone runs 0 except at most 64 query rows at d = 128.
+ * Returns -1 on invalid sizes.
  */
 int streamkl_bwd_algorithm(int B, int H, int NQ, int NK, int d, int causal, int want_grad1);
 

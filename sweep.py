@@ -93,7 +93,12 @@ def sweep_algo(reps: int):
                                            (2, 16, 8192, 8192, False, False),
                                            (1, 16, 16384, 16384, True, False),
                                            (2, 16, 4096, 4096, False, True),
-                                           (4, 16, 2048, 8192, True, False)]]
+                                           (4, 16, 2048, 8192, True, False),
+                                           (4, 32, 256, 8192, False, False),
+                                           (4, 32, 512, 2048, False, False),
+                                           (4, 32, 512, 16384, False, False),
+                                           (2, 16, 1024, 32768, False, False),
+                                           (1, 16, 16384, 16384, False, False)]]
     print("| workload | sets | separate ms | fused ms | faster | library's choice |")
     print("|---|---|---:|---:|---|---|")
     for w in shapes:

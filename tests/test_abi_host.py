@@ -146,16 +146,19 @@ def test_workspace_sizes(lib):
 def test_automatic_backward_choice(lib):
     lib.streamkl_set_bwd_algorithm(-1)
     # separate kernels unless the query rows fit the fused short-sweep kernel
-    # (at most 64 at d = 128) or, at d = 64 with one gradient set, a CTA has
-    # at least four query blocks (512 rows)
+    # (at most 64 at d = 128) or, with one gradient set, a CTA of the fused
+    # per-key-tile kernel sweeps enough query rows: 512 at d = 64, at d = 128
+    # 512 without the mask and 1,024 with it
     for args in [(1, 32, 65536, 65536, 128, 1, 1), (4, 32, 65, 65536, 128, 1, 0),
                  (4, 32, 512, 131072, 128, 1, 0), (4, 32, 256, 65536, 128, 1, 0),
-                 (4, 32, 256, 65536, 64, 1, 0), (4, 32, 64, 65536, 64, 1, 0),
-                 (1, 8, 16384, 16384, 64, 0, 1)]:
+                 (4, 32, 1023, 65536, 128, 1, 0), (4, 32, 256, 8192, 128, 0, 0),
+                 (2, 16, 4096, 4096, 128, 0, 1), (4, 32, 256, 65536, 64, 1, 0),
+                 (4, 32, 64, 65536, 64, 1, 0), (1, 8, 16384, 16384, 64, 0, 1)]:
         assert lib.streamkl_bwd_algorithm(*args) == 0, args
     for args in [(4, 32, 64, 65536, 128, 1, 0), (1, 8, 1, 4096, 128, 0, 1),
                  (2, 2, 17, 300, 128, 1, 1), (4, 32, 512, 131072, 64, 1, 0),
-                 (1, 8, 16384, 16384, 64, 0, 0)]:
+                 (1, 8, 16384, 16384, 64, 0, 0), (2, 16, 4096, 4096, 128, 0, 0),
+                 (4, 32, 512, 2048, 128, 0, 0), (4, 32, 1024, 65536, 128, 1, 0)]:
         assert lib.streamkl_bwd_algorithm(*args) == 1, args
 
 

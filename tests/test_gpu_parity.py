@@ -372,6 +372,18 @@ def test_fused_d64_backward_automatic(NQ, NK, causal):
     full_check(w, seed=NQ + NK, grad1=False)
 
 
+@pytest.mark.parametrize("NQ,NK,causal", [(600, 777, False), (1100, 1300, True), (512, 4096, False)])
+def test_fused_d128_backward_automatic(NQ, NK, causal):
+    """At d = 128 with one gradient set the library picks the fused per-key-tile
+    kernel (64-row query steps, K in TMEM for the score GEMMs, dQ through TMA
+    bulk reductions from two alternating staging tiles) from 512 query rows
+    without the mask and 1,024 with it: ragged shapes against the oracle."""
+    w = synthetic.custom(f"fused128_{NQ}x{NK}", B=2, H=2, NQ=NQ, NK=NK, d=128, causal=causal,
+                         noise=0.4, grad1=False)
+    assert binding.bwd_algorithm(w.B, w.H, w.NQ, w.NK, w.d, w.causal, False) == binding.BWD_FUSED
+    full_check(w, seed=NQ + 3 * NK, grad1=False)
+
+
 @pytest.mark.parametrize("B,H,NQ,NK,causal,sets", SHORT)
 def test_short_sweep_fused_backward(B, H, NQ, NK, causal, sets):
     """The fused algorithm's short-sweep kernel (at most 64 query rows, d =
@@ -549,10 +561,11 @@ def _rows(n, k, seed):
     return r
 
 
-def test_mid_workload_full_size():
+@pytest.mark.parametrize("algo", ALGOS)
+def test_mid_workload_full_size(algo):
     w = synthetic.WORKLOADS["mid"]
     sampled_check(w, heads=[(0, 0), (1, 15)], rows=_rows(w.NQ, 384, 1),
-                  key_sets=[np.arange(0, 128), np.arange(w.NK - 200, w.NK)])
+                  key_sets=[np.arange(0, 128), np.arange(w.NK - 200, w.NK)], algo=algo)
 
 
 def test_stress_workload_full_size():
