@@ -87,10 +87,10 @@ struct Fused128Layout {
   static constexpr int OFF_STG = OFF_DS + NSETS * DST;
   static constexpr int OFF_TAB = OFF_STG + STG;
   static constexpr int OFF_BAR = OFF_TAB + STAGES * TAB;
-  // k_full, q_full[S], q_empty[S], t_full, t_free, ds_full, ds_free, dq_full,
-  // dq_free, dk_full, stg_full, stg_empty, drain, kt_full, then stg_full and
-  // stg_empty of staging tile 1
-  static constexpr int NBAR = 1 + 2 * STAGES + 13;
+  // k_full, q_full[S], q_empty[S], t_full, t_free, ds_full, dq_full, dq_free,
+  // dk_full, stg_full, stg_empty, drain, kt_full, then stg_full and stg_empty
+  // of staging tile 1
+  static constexpr int NBAR = 1 + 2 * STAGES + 12;
   static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_MISC + 16;
   static constexpr int ALLOC = BYTES + 1024;
@@ -139,16 +139,19 @@ __global__ void __launch_bounds__(kF2Threads, 1)
   auto q_full = [&](int s) { return bar0 + 8u * (1 + s); };
   auto q_empty = [&](int s) { return bar0 + 8u * (1 + L::STAGES + s); };
   const uint32_t t_full = bar0 + 8u * (1 + 2 * L::STAGES);
-  const uint32_t t_free = t_full + 8, ds_full = t_full + 16, ds_free = t_full + 24;
-  const uint32_t dq_full = t_full + 32, dq_free = t_full + 40, dk_full = t_full + 48;
-  const uint32_t stg_full = t_full + 56, stg_empty = t_full + 64, drain = t_full + 72;
-  const uint32_t kt_full = t_full + 80;  // K rows copied into TMEM
-  static_assert(1 + 2 * L::STAGES + 13 == L::NBAR, "barrier region holds every barrier");
+  const uint32_t t_free = t_full + 8, ds_full = t_full + 16;
+  // dq_full: the step's dQ^T GEMMs, the last readers of its dS tiles, are
+  // done (one commit serves both: a commit costs the tensor pipe about as
+  // much as an MMA)
+  const uint32_t dq_full = t_full + 24, dq_free = t_full + 32, dk_full = t_full + 40;
+  const uint32_t stg_full = t_full + 48, stg_empty = t_full + 56, drain = t_full + 64;
+  const uint32_t kt_full = t_full + 72;  // K rows copied into TMEM
+  static_assert(1 + 2 * L::STAGES + 12 == L::NBAR, "barrier region holds every barrier");
   // staging use u (one per set and step, then one per set for dK) goes
   // through tile u % NSTG
   constexpr int NSTG = L::NSTG;
-  auto stg_full_b = [&](int u) { return u % NSTG ? t_full + 88 : stg_full; };
-  auto stg_empty_b = [&](int u) { return u % NSTG ? t_full + 96 : stg_empty; };
+  auto stg_full_b = [&](int u) { return u % NSTG ? t_full + 80 : stg_full; };
+  auto stg_empty_b = [&](int u) { return u % NSTG ? t_full + 88 : stg_empty; };
   auto stg_tile = [&](int u) { return sb + (u % NSTG ? L::OFF_STG1 : L::OFF_STG); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
@@ -176,7 +179,6 @@ __global__ void __launch_bounds__(kF2Threads, 1)
       mbar_init(t_full, 1);
       mbar_init(t_free, kF2SoftmaxWarps);
       mbar_init(ds_full, kF2SoftmaxWarps);
-      mbar_init(ds_free, 1);
       mbar_init(dq_full, 1);
       mbar_init(dq_free, kF2SoftmaxWarps);
       mbar_init(dk_full, 1);
@@ -379,7 +381,6 @@ __global__ void __launch_bounds__(kF2Threads, 1)
                      smem_desc_sw128(ds + kk * 2048, 8192, 1024), id_dq, kk > 0);
         }
         mma_commit(dq_full);
-        mma_commit(ds_free);
       }
       mma_commit(dk_full);  // after every MMA of this CTA (dK complete)
       mma_commit(drain);
@@ -560,7 +561,7 @@ __global__ void __launch_bounds__(kF2Threads, 1)
         }
       }
       // the previous step's gradient GEMMs have read the dS tiles
-      if (j > 0 && !(ok = __all_sync(0xffffffffu, wait_bounded(ds_free, (j - 1) & 1, wc)))) break;
+      if (j > 0 && !(ok = __all_sync(0xffffffffu, wait_bounded(dq_full, (j - 1) & 1, wc)))) break;
       // row r of each dS tile: 128 bytes = 64 queries; this thread's 32 bytes
       // are 16-byte chunks 2 grp and 2 grp + 1, swizzled by the row
       const uint32_t row = sb + L::OFF_DS + static_cast<uint32_t>(r * 128);
