@@ -656,7 +656,7 @@ def gpu_arm(args, w):
                        "causal": w.causal, "grad1": w.grad1, "splits": splits,
                        "bwd_algorithm": "separate" if separate else "fused",
                        "flop_convention": "4 NQ NK d fwd + 8 NQ NK d bwd per head, halved for causal",
-                       "l2": "inputs (2 GiB) larger than L2; no flush", "parallelism": f"replicas x{world}"},
+                       "l2": l2_note(B, H, NQ, NK, d), "parallelism": f"replicas x{world}"},
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": f_fwd / (fwd_ms * 1e-3) / 1e12,
             "bwd_tflops_metric": f_bwd_metric / (bwd_ms * 1e-3) / 1e12,
@@ -786,6 +786,14 @@ def e2e_measure(args, w, binding, synthetic, dev, rank, step_flops, world):
                        "two device slots: a group's inputs are copied in on one stream and its "
                        "results out on another while the neighbouring group computes",
             "api": "attention_kl_loss_gb300.streamkl_fwd/streamkl_bwd (ctypes over the C ABI)"}
+
+
+def l2_note(B, H, NQ, NK, d):
+    """How the timed steps relate to the 129 MB L2: the four bf16 inputs'
+    size (no flush runs between steps)."""
+    in_bytes = 2 * 2 * B * H * (NQ + NK) * d
+    rel = "larger" if in_bytes > 129e6 else "not larger"
+    return f"inputs ({in_bytes / 1e6:.0f} MB) {rel} than the 129 MB L2; no flush"
 
 
 def main(argv=None):
