@@ -323,7 +323,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
                    smem_desc_sw128(kbase + L::TILE + koff, 16, 1024), idesc, k > 0);
         }
         mma_commit(s_full(slot));
-        mma_commit(kv_empty(s));
       }
       mma_commit(drain);
       wait_drain(drain, 0, timeout_ns);
@@ -342,6 +341,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       const int slot = it & 1;
       const uint32_t sph = (it >> 1) & 1;
       if (!wait_bounded(s_full(slot), sph, wc)) break;
+      // the S GEMMs were the K stage's only readers
+      if (warp == 2 && lane == 0) mbar_arrive(kv_empty(it % L::STAGES));
       tc_fence_after();
       float a[32], b[32];
       const uint32_t ta = lane_base + slot * 256;
