@@ -185,9 +185,10 @@ bool short_sweep(int NQ, int d) { return d == 128 && NQ <= skl::kShortMaxQ; }
 // bound d = 64, the fused kernel once; below 512 rows a CTA has only one to
 // three query blocks and the persistent dK kernel wins); the fused d = 128
 // kernel with one gradient set from 512 query rows on without a mask and from
-// 1,024 with the causal one (non-causal 1.02-1.12x, causal 1.00-1.02x; at 512
-// causal rows, the split-K shape, and at 256 rows the separate kernels are
-// faster); the separate kernels everywhere else, both gradient sets included.
+// 1,024 with the causal one (non-causal 1.03-1.11x, causal 1.02-1.03x; at 512
+// causal rows, the split-K shape, the two are level, and at 256 rows the
+// separate kernels are faster); the separate kernels everywhere else, both
+// gradient sets included.
 int bwd_algo_impl(int B, int H, int NQ, int NK, int d, int causal, int grad1) {
   const int forced = forced_algo();
   if (forced >= 0) return forced;
