@@ -294,8 +294,15 @@ __global__ void __launch_bounds__(kF2Threads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && n > 0) {
       // the whole of TMEM is this CTA's, so its base address is 0; a
-      // compile-time base keeps the MMA operand addresses constants
+      // compile-time base keeps the MMA operand addresses constants (checked
+      // in every build: a nonzero base stops the CTA with a device-check
+      // status instead of issuing MMAs to the wrong columns)
       constexpr uint32_t tmem = 0;
+      const bool base_zero = *tmem_slot == 0u;
+      if (!base_zero) {
+        *abort_flag = 1;
+        atomicCAS(dev_status, 0, kStatusDeviceCheck);
+      }
       constexpr uint32_t id_t = idesc_bf16(kBlockN, STEP, 0, 0);  // T = K Q^T
       constexpr uint32_t id_dk = idesc_bf16(kBlockN, D, 0, 1);    // dK = dS Q
       constexpr uint32_t id_dq = idesc_bf16(D, STEP, 1, 1);       // dQ^T = K^T dS
@@ -303,8 +310,7 @@ __global__ void __launch_bounds__(kF2Threads, 1)
                 check_tmem(ck, tmem + L::COL_DK, 128, L::NSETS * D, __LINE__) &&
                 check_tmem(ck, tmem + L::COL_DQ, 128, L::NSETS * STEP, __LINE__) &&
                 (!L::KTM || check_tmem(ck, tmem + L::COL_K, 128, D, __LINE__)) &&
-                dcheck(ck, *tmem_slot == 0u, __LINE__) &&
-                wait_bounded(k_full, 0, wc) && (!L::KTM || wait_bounded(kt_full, 0, wc));
+                base_zero && wait_bounded(k_full, 0, wc) && (!L::KTM || wait_bounded(kt_full, 0, wc));
       const uint32_t k1s = sb + L::OFF_K, k2s = k1s + L::KT;
       // T of step j: two K-major GEMMs (A = K tile, B = Q tile), k-steps interleaved
       auto issue_t = [&](int j) {
