@@ -19,10 +19,16 @@
 //                split-K partials. Four warps per scheduler hide the exp2/FMA
 //                latency, and column pairs use the packed f32x2 FMA path.
 //
-// Numerics: exponentials are base 2 with the reference maximum kept in log2
-// units (r = m * scale * log2 e). The reference is only moved when a chunk's
-// maximum exceeds it by more than kTau (=8, so no term exceeds 2^8); moving it
-// rescales l and acc, so the result is the same for any reference.
+// Numerics: exponentials are base 2 with a reference kept in log2 units
+// (r = m * scale * log2 e). A row's first chunk sets it to that chunk's
+// maximum. Later chunks are folded against it directly, with no maximum
+// taken: when a chunk's terms sum to F > 2^kTau (=2^8) the reference moves up
+// by log2 F, which brings that sum to 1, so no accumulated term exceeds 2^8.
+// A term that leaves the fp32 range (a logit more than 128 log2 units above
+// the reference) leaves NaN in the row's state; a CTA with such a row sweeps
+// its key tiles a second time, folding every chunk from its maximum (moved
+// only when that exceeds the reference by more than kTau). Moving the
+// reference rescales l and acc, so the result is the same for any reference.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -35,6 +41,12 @@ constexpr int kGroups = 4;        // softmax column groups (warpgroups)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kTau = 8.0f;
+constexpr float kSumMax = 256.0f;  // 2^kTau
+
+// CTA-wide barrier 0 that the threads of one warp may reach from different
+// code paths (the roles end their first sweep in different branches); the
+// non-aligned form of the instruction allows that, __syncthreads does not.
+__device__ __forceinline__ void cta_barrier_divergent() { asm volatile("barrier.sync 0;" ::: "memory"); }
 
 template <int D>
 struct FwdLayout {
@@ -58,10 +70,14 @@ struct RowState {
 };
 
 // Fold one 32-column chunk of a row into the state. a = S1 row values, b = S2
-// (raw dot products). With MASK, keys >= lim are excluded.
+// (raw dot products). With MASK, keys >= lim are excluded. Unless from_max,
+// a row with finite references folds the chunk against them; a term that
+// overflows there leaves NaN in l1 or l2 (inf times the 1/inf rescale), for
+// the sweep from the maxima to rebuild. Otherwise the chunk's maximum moves
+// the references first.
 template <bool MASK>
 __device__ __forceinline__ void fold_chunk(float (&a)[32], float (&b)[32], int key0, int lim,
-                                           float c, RowState& st) {
+                                           float c, RowState& st, bool from_max) {
   if (MASK) {
 #pragma unroll
     for (int k = 0; k < 32; ++k) {
@@ -70,6 +86,48 @@ __device__ __forceinline__ void fold_chunk(float (&a)[32], float (&b)[32], int k
         b[k] = -INFINITY;
       }
     }
+  }
+  if (!from_max && st.r1 != -INFINITY && st.r2 != -INFINITY) {
+    const float2 c2 = make_float2(c, c), m1 = make_float2(-1.f, -1.f);
+    const float2 nr1 = make_float2(-st.r1, -st.r1), nr2 = make_float2(-st.r2, -st.r2);
+    float2 l1p[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 l2p[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 ap[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int k = 0; k < 32; k += 2) {
+      const float2 s1 = make_float2(a[k], a[k + 1]), s2 = make_float2(b[k], b[k + 1]);
+      const float2 x1 = __ffma2_rn(s1, c2, nr1), x2 = __ffma2_rn(s2, c2, nr2);
+      const float2 p1 = make_float2(ex2(x1.x), ex2(x1.y));
+      const float2 p2 = make_float2(ex2(x2.x), ex2(x2.y));
+      const int h = (k >> 1) & 1;
+      l1p[h] = __fadd2_rn(l1p[h], p1);
+      l2p[h] = __fadd2_rn(l2p[h], p2);
+      float2 dd = __ffma2_rn(s2, m1, s1);  // s1 - s2
+      if (MASK) {
+        if (a[k] == -INFINITY) dd.x = 0.f;
+        if (a[k + 1] == -INFINITY) dd.y = 0.f;
+      }
+      ap[h] = __ffma2_rn(p1, dd, ap[h]);
+    }
+    const float2 l1s = __fadd2_rn(l1p[0], l1p[1]), l2s = __fadd2_rn(l2p[0], l2p[1]);
+    const float2 as = __fadd2_rn(ap[0], ap[1]);
+    const float f1 = l1s.x + l1s.y, f2 = l2s.x + l2s.y, fa = as.x + as.y;
+    if (f1 > kSumMax) {  // reference up by log2 f1: the state and this chunk scale by 1/f1
+      const float inv = 1.f / f1;
+      st.r1 += __log2f(f1);
+      st.l1 = (st.l1 + f1) * inv;
+      st.acc = (st.acc + fa) * inv;
+    } else {
+      st.l1 += f1;
+      st.acc += fa;
+    }
+    if (f2 > kSumMax) {
+      st.r2 += __log2f(f2);
+      st.l2 = (st.l2 + f2) * (1.f / f2);
+    } else {
+      st.l2 += f2;
+    }
+    return;
   }
   float x1[11], x2[11];
 #pragma unroll
@@ -192,12 +250,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gb + L::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 4);
   volatile int* skip_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 8);
+  volatile int* redo_flag = reinterpret_cast<volatile int*>(gb + L::OFF_MISC + 12);
 
   // debug build: the layout's regions (TMEM fields are set once allocated)
   CheckCtx ck{sb, sb + L::OFF_BAR, sb + L::OFF_BAR, sb + L::OFF_BAR + L::NBAR * 8, 0, 0,
               abort_flag, dev_status};
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    *redo_flag = 0;
     bool lay_ok = true;
     if (kDeviceChecks) {  // every barrier address inside the barrier region
       lay_ok = check_bar(ck, q_full, __LINE__) && check_bar(ck, drain, __LINE__);
@@ -267,10 +327,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         tma_load_3d(sb + L::OFF_Q2 + kb * 16384, &tm_q2, q_full, kb * 64, sv.q_row0 + qb * kBlockM,
                     sv.z);
       }
-      int it = 0;
-      for (; it < n_iter; ++it) {
-        const int s = it % L::STAGES;
-        const uint32_t ph = (it / L::STAGES) & 1;
+      int g = 0;  // key tiles loaded so far, over both sweeps
+      for (int pass = 0; pass < 2; ++pass) {
+      if (pass == 1) {
+        // a second sweep when a chunk overflowed against its reference
+        cta_barrier_divergent();
+        if (!*redo_flag) break;
+      }
+      for (int it = 0; it < n_iter; ++it, ++g) {
+        const int s = g % L::STAGES;
+        const uint32_t ph = (g / L::STAGES) & 1;
         if (!wait_bounded(kv_empty(s), ph ^ 1, wc)) break;
         const int krow = sv.k_row0 + (t_begin + it) * kBlockN;
         const uint32_t dst = sb + L::OFF_K + s * 2 * L::TILE;
@@ -290,10 +356,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
           tma_load_3d(dst + L::TILE + kb * 16384, &tm_k2, kv_full(s), kb * 64, krow, sv.z);
         }
       }
+      }
       // Let every copy this thread issued land before the CTA can exit.
       wait_drain(q_full, 0, timeout_ns);
-      for (int j = max(0, it - L::STAGES); j < it; ++j)
+      for (int j = max(0, g - L::STAGES); j < g; ++j)
         wait_drain(kv_full(j % L::STAGES), (j / L::STAGES) & 1, timeout_ns);
+    } else {
+      cta_barrier_divergent();  // the first sweep's end (every thread takes part once)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -301,17 +370,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       constexpr uint32_t idesc = idesc_bf16(kBlockM, kBlockN, 0, 0);
       bool ok = wait_bounded(q_full, 0, wc);
       tc_fence_after();
-      for (int it = 0; ok && it < n_iter; ++it) {
-        const int s = it % L::STAGES;
-        const uint32_t ph = (it / L::STAGES) & 1;
-        const int slot = it & 1;
-        const uint32_t sph = (it >> 1) & 1;
-        if (!wait_bounded(kv_full(s), ph, wc)) break;
-        if (!wait_bounded(s_empty(slot), sph ^ 1, wc)) break;
+      int g = 0;  // key tiles so far, over both sweeps
+      for (int pass = 0; pass < 2; ++pass) {
+      if (pass == 1) {
+        cta_barrier_divergent();  // the first sweep's end
+        if (!*redo_flag) break;
+      }
+      for (int it = 0; ok && it < n_iter; ++it, ++g) {
+        const int s = g % L::STAGES;
+        const uint32_t ph = (g / L::STAGES) & 1;
+        const int slot = g & 1;
+        const uint32_t sph = (g >> 1) & 1;
+        if (!(ok = wait_bounded(kv_full(s), ph, wc))) break;
+        if (!(ok = wait_bounded(s_empty(slot), sph ^ 1, wc))) break;
         tc_fence_after();
         const uint32_t kbase = sb + L::OFF_K + s * 2 * L::TILE;
         const uint32_t d1 = tmem + slot * 256, d2 = d1 + 128;
-        if (!check_tmem(ck, d1, 128, 256, __LINE__)) break;
+        if (!(ok = check_tmem(ck, d1, 128, 256, __LINE__))) break;
         // the two GEMMs' k-steps interleaved: independent accumulators keep
         // the tensor pipe busy where one dependent chain would stall it
 #pragma unroll
@@ -324,8 +399,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
         }
         mma_commit(s_full(slot));
       }
+      }
       mma_commit(drain);
       wait_drain(drain, 0, timeout_ns);
+    } else {
+      cta_barrier_divergent();  // the first sweep's end (every thread takes part once)
     }
   } else if (warp >= 2) {
     // ------------------------------------------------------------ softmax / KL
@@ -335,30 +413,40 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
     const int qrow = qb * kBlockM + r;
     const float c = scale * kLog2e;
     const int lim = causal ? min(nk, qrow + 1 + off) : nk;  // keys < lim visible
-    RowState st{-INFINITY, 0.f, -INFINITY, 0.f, 0.f};
+    RowState st;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + grp * 32;
-    for (int it = 0; it < n_iter; ++it) {
-      const int slot = it & 1;
-      const uint32_t sph = (it >> 1) & 1;
-      if (!wait_bounded(s_full(slot), sph, wc)) break;
-      // the S GEMMs were the K stage's only readers
-      if (warp == 2 && lane == 0) mbar_arrive(kv_empty(it % L::STAGES));
-      tc_fence_after();
-      float a[32], b[32];
-      const uint32_t ta = lane_base + slot * 256;
-      if (!(check_tmem(ck, ta, 32, 32, __LINE__) && check_tmem(ck, ta + 128, 32, 32, __LINE__)))
-        break;
-      tmem_ld32(ta, a);
-      tmem_ld32(ta + 128, b);
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty(slot));
-      const int key0 = (t_begin + it) * kBlockN + grp * 32;
-      if (key0 + 32 <= lim)
-        fold_chunk<false>(a, b, key0, lim, c, st);
-      else
-        fold_chunk<true>(a, b, key0, lim, c, st);
+    int g = 0;  // key tiles so far, over both sweeps
+    for (int pass = 0; pass < 2; ++pass) {
+      if (pass == 1) {
+        cta_barrier_divergent();  // the first sweep's end: did any chunk overflow?
+        if (!*redo_flag) break;
+      }
+      st = RowState{-INFINITY, 0.f, -INFINITY, 0.f, 0.f};
+      for (int it = 0; it < n_iter; ++it, ++g) {
+        const int slot = g & 1;
+        const uint32_t sph = (g >> 1) & 1;
+        if (!wait_bounded(s_full(slot), sph, wc)) break;
+        // the S GEMMs were the K stage's only readers
+        if (warp == 2 && lane == 0) mbar_arrive(kv_empty(g % L::STAGES));
+        tc_fence_after();
+        float a[32], b[32];
+        const uint32_t ta = lane_base + slot * 256;
+        if (!(check_tmem(ck, ta, 32, 32, __LINE__) && check_tmem(ck, ta + 128, 32, 32, __LINE__)))
+          break;
+        tmem_ld32(ta, a);
+        tmem_ld32(ta + 128, b);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty(slot));
+        const int key0 = (t_begin + it) * kBlockN + grp * 32;
+        if (key0 + 32 <= lim)
+          fold_chunk<false>(a, b, key0, lim, c, st, pass > 0);
+        else
+          fold_chunk<true>(a, b, key0, lim, c, st, pass > 0);
+      }
+      // an overflowed chunk left NaN in l1 or l2 (inf times the 1/inf rescale)
+      if (pass == 0 && !(st.l1 == st.l1 && st.l2 == st.l2)) *redo_flag = 1;
     }
     // merge the column groups' states of each row into group 0
     float* xch = reinterpret_cast<float*>(gb + L::OFF_XCH);
@@ -655,10 +743,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1)
       // the even CTA's barrier; the arrival publishes no memory, so relaxed
       if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(s_empty(slot), 0));
       const int key0 = it * kBlockN + grp * 32;
+      // (the pair kernel folds every chunk from its maximum)
       if (key0 + 32 <= lim)
-        fold_chunk<false>(a, b, key0, lim, c, st);
+        fold_chunk<false>(a, b, key0, lim, c, st, true);
       else
-        fold_chunk<true>(a, b, key0, lim, c, st);
+        fold_chunk<true>(a, b, key0, lim, c, st, true);
     }
     float* xch = reinterpret_cast<float*>(gb + L::OFF_XCH);
     if (grp > 0) {
