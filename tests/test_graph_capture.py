@@ -68,6 +68,7 @@ CASES = [
     ("split forward d64", dict(B=1, H=4, NQ=64, NK=8192, d=64, causal=True)),
     ("short sweep", dict(B=2, H=8, NQ=48, NK=4000, d=128, causal=True, grad1=True)),
     ("fused d64", dict(B=1, H=2, NQ=640, NK=700, d=64, causal=True)),
+    ("fused d128", dict(B=1, H=2, NQ=600, NK=650, d=128, causal=False)),
 ]
 
 
@@ -94,9 +95,9 @@ def _close(got, want, what, atomic_dq):
 @pytest.mark.parametrize("name,shape", CASES, ids=[c[0] for c in CASES])
 def test_captured_step_with_binding_allocations(name, shape):
     """Outputs and workspace allocated by the binding inside the capture (from
-    the graph's memory pool), on the separate, split-forward and short-sweep
-    paths; the short-sweep dQ is summed with fp32 reductions, so it matches
-    to rounding."""
+    the graph's memory pool), on the separate, split-forward, short-sweep and
+    per-key-tile fused paths; the fused paths sum dQ with fp32 reductions, so
+    it matches to rounding."""
     w = synthetic.custom(name.replace(" ", "_"), noise=0.3, **shape)
     dev = torch.device("cuda")
     ins = synthetic.make_inputs(w, 41, dev)
@@ -104,6 +105,8 @@ def test_captured_step_with_binding_allocations(name, shape):
     fused = binding.bwd_algorithm(w.B, w.H, w.NQ, w.NK, w.d, w.causal, w.grad1) == binding.BWD_FUSED
     if name == "split forward d64":
         assert binding.choose_splits(w.B, w.H, w.NQ, w.NK, w.d, w.causal) > 1
+    if name.startswith("fused"):
+        assert fused
 
     eager = _step(w, ins, status)  # also loads every kernel before the capture
     torch.cuda.synchronize()
