@@ -467,13 +467,14 @@ def test_peaked_teacher_independent_student(d, algo):
 # the oracle evaluates exp on masked entries too and discards them; with these
 # logits that overflows harmlessly
 @pytest.mark.filterwarnings("ignore:overflow encountered in exp")
-@pytest.mark.parametrize("causal", [False, True])
-def test_forward_reference_moves_and_overflow(causal):
+@pytest.mark.parametrize("causal,splits", [(False, 0), (True, 0), (True, 3)])
+def test_forward_reference_moves_and_overflow(causal, splits):
     """Later key tiles far above a row's first chunk: key 150 (K1) / 200 (K2)
     some 40-50 log2 units above it, which moves the forward's reference by the
     chunk sum, and key 300 (K1) / 600 (K2) over 1,000 log2 units above it,
-    which overflows fp32 and sends the chunk back to the maximum-based fold
-    from the tile still in TMEM. KL and both LSEs against the oracle."""
+    which overflows fp32 and makes the CTA sweep its key tiles again from the
+    chunk maxima (with key splits: the CTA of the split holding the key).
+    KL and both LSEs against the oracle."""
     w = synthetic.custom("jumps", B=1, H=2, NQ=700, NK=700, d=64, causal=causal, noise=0.3)
     q1, k1, q2, k2, _ = synthetic.make_inputs(w, 17, torch.device("cuda"))
     gen = torch.Generator().manual_seed(17)
@@ -487,7 +488,8 @@ def test_forward_reference_moves_and_overflow(causal):
     k2[:, :, 200] = u
     k2[:, :, 600] = 30 * u
     status = binding.new_status(torch.device("cuda"))
-    kl, l1, l2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, dev_status=status)
+    kl, l1, l2 = binding.streamkl_fwd(q1, k1, q2, k2, w.scale, w.causal, num_splits=splits,
+                                      dev_status=status)
     binding.raise_on_device_status(status, w.name)
     h = [host(t) for t in (q1, k1, q2, k2)]
     okl, ol1, ol2 = orc.forward(*h, w.scale, w.causal)
